@@ -1,0 +1,299 @@
+/*
+ * oracle.c -- plain fp64 CPU reference for decode attention over a paged KV cache,
+ * for the per-step KV append, and for the gather of one request's blocks into a
+ * contiguous transfer buffer.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's CPU
+ * baseline load this file. It shares no code, header, table or helper with the CUDA
+ * library; it is written from the problem statement alone:
+ *
+ *  - Decode step (page "Disaggregated LLM Serving: from PD disaggregation to attention
+ *    offload", sec. 1 "starting from autoregressive generation", item 2 of the second
+ *    list): each decode step reads the whole cached K/V history of the request and
+ *    appends the new token's K/V to it.
+ *  - Paged layout (page "From PagedAttention to Prefill-Decode disaggregation", sec. 2.2
+ *    steps 1-2): the cache is split into fixed-size physical blocks, each holding the K
+ *    and V of a fixed number of tokens; a per-request table maps logical block i of the
+ *    request to a physical block, and the physical blocks need not be contiguous.
+ *  - Shared prefixes (same page, sec. 2.3): several requests may map to the same
+ *    physical blocks; attention only reads them.
+ *  - Request-level transfer of the KV (page on goodput and PD disaggregation,
+ *    0539edu.com, sec. 5.4 "request-level granularity"): after prefill the whole KV of
+ *    a request is sent in one piece, which needs it gathered into one buffer.
+ *
+ * Attention is the plain definition, with no online or split softmax:
+ *      s_t = scale * sum_d q[d] * K_t[d]            for t < L
+ *      p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
+ *      out = sum_t p_t * V_t
+ * Everything is computed in double; stored bf16/fp32 inputs are upcast exactly.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - Cache tensors are dense row-major [num_blocks, block_size, H_kv, D].
+ *  - Query head h reads kv-head h / (H / H_kv) (contiguous grouping for GQA).
+ *  - Token t of request b lives in physical block block_tables[b][t / block_size] at
+ *    row t % block_size.
+ *  - context_lens counts the tokens after this step's append.
+ *  - A request with context length 0 yields a zero row; a negative length, a length
+ *    beyond the table's capacity or a block id outside [0, num_blocks) yields NaN rows
+ *    for that request and the status ORC_ERR_DATA.
+ *
+ * The functions oracle_attention_partial and oracle_lse_combine exist only so that a
+ * test can show that the split-and-merge arithmetic gives back the plain definition.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_DATA = 4 };
+
+static size_t orc_elem_size(int dtype) { return dtype == ORC_BF16 ? 2u : 4u; }
+
+static int orc_dtype_ok(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF16; }
+
+/* Exact upcast of stored element idx. A bf16 value is the upper 16 bits of a binary32. */
+static double orc_load(const void* base, size_t idx, int dtype) {
+  if (dtype == ORC_BF16) {
+    uint16_t h;
+    memcpy(&h, (const char*)base + idx * 2u, 2u);
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, 4u);
+    return (double)f;
+  }
+  float f;
+  memcpy(&f, (const char*)base + idx * 4u, 4u);
+  return (double)f;
+}
+
+int oracle_version(void) { return 1; }
+
+/*
+ * KV append: for each request b whose slot s = slot_mapping[b] is >= 0, write the
+ * new token's K and V (H_kv x D elements each) to block s / block_size, row
+ * s % block_size. Bitwise copy. A slot >= num_blocks * block_size is an error and is
+ * skipped; a negative slot means "no token" (padding) and is skipped silently.
+ */
+int oracle_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int32_t* slot_mapping, int B, int H_kv, int D, int block_size,
+                     int num_blocks, int dtype) {
+  if (B < 0 || H_kv <= 0 || D <= 0 || block_size <= 0 || num_blocks <= 0 || !orc_dtype_ok(dtype))
+    return ORC_ERR_ARG;
+  const size_t e = orc_elem_size(dtype);
+  const size_t row_bytes = (size_t)H_kv * (size_t)D * e;
+  int status = ORC_OK;
+  for (int b = 0; b < B; ++b) {
+    const int32_t s = slot_mapping[b];
+    if (s < 0) continue;
+    if ((int64_t)s >= (int64_t)num_blocks * block_size) {
+      status = ORC_ERR_DATA;
+      continue;
+    }
+    const int64_t block = s / block_size;
+    const int64_t offset = s % block_size;
+    const size_t dst = ((size_t)block * (size_t)block_size + (size_t)offset) * row_bytes;
+    memcpy((char*)k_cache + dst, (const char*)k_new + (size_t)b * row_bytes, row_bytes);
+    memcpy((char*)v_cache + dst, (const char*)v_new + (size_t)b * row_bytes, row_bytes);
+  }
+  return status;
+}
+
+/*
+ * KV pack: out[t, 0, h, :] = K of logical token t, out[t, 1, h, :] = V of token t, for
+ * t < context_len, with token t found through block_table_row as for attention.
+ * Bitwise copy into a dense [context_len, 2, H_kv, D] buffer.
+ */
+int oracle_kv_pack_blocks(void* out, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table_row, int context_len, int H_kv, int D,
+                          int block_size, int num_blocks, int dtype) {
+  if (context_len < 0 || H_kv <= 0 || D <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      !orc_dtype_ok(dtype))
+    return ORC_ERR_ARG;
+  const size_t e = orc_elem_size(dtype);
+  const size_t row_bytes = (size_t)H_kv * (size_t)D * e;
+  for (int t = 0; t < context_len; ++t) {
+    const int32_t block = block_table_row[t / block_size];
+    if (block < 0 || block >= num_blocks) return ORC_ERR_DATA;
+    const size_t src = ((size_t)block * (size_t)block_size + (size_t)(t % block_size)) * row_bytes;
+    char* dst = (char*)out + (size_t)t * 2u * row_bytes;
+    memcpy(dst, (const char*)k_cache + src, row_bytes);
+    memcpy(dst + row_bytes, (const char*)v_cache + src, row_bytes);
+  }
+  return ORC_OK;
+}
+
+/*
+ * Gather the K and V of kv-head hk of request b into contiguous [L, D] arrays of
+ * doubles. Returns 0, or -1 when a block id is out of range.
+ */
+static int orc_gather(double* Kc, double* Vc, const void* k_cache, const void* v_cache,
+                      const int32_t* table_row, int L, int hk, int H_kv, int D, int block_size,
+                      int num_blocks, int kv_dtype) {
+  for (int t = 0; t < L; ++t) {
+    const int32_t block = table_row[t / block_size];
+    if (block < 0 || block >= num_blocks) return -1;
+    const size_t row = (size_t)block * (size_t)block_size + (size_t)(t % block_size);
+    const size_t base = (row * (size_t)H_kv + (size_t)hk) * (size_t)D;
+    for (int d = 0; d < D; ++d) {
+      Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype);
+      Vc[(size_t)t * D + d] = orc_load(v_cache, base + d, kv_dtype);
+    }
+  }
+  return 0;
+}
+
+static void orc_fill_rows(double* out, int b, int H, int D, double value) {
+  for (size_t i = 0; i < (size_t)H * D; ++i) out[(size_t)b * H * D + i] = value;
+}
+
+/*
+ * Decode attention over the paged cache. out is [B, H, D] doubles. q is [B, H, D] in
+ * q_dtype; caches are [num_blocks, block_size, H_kv, D] in kv_dtype; block_tables is
+ * [B, max_blocks]; context_lens is [B]. scale is the binary32 value a caller passes to
+ * the kernel, used upcast to double. num_threads <= 0 uses the OpenMP default.
+ */
+int oracle_paged_decode_attention(double* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int max_blocks, const int32_t* context_lens, int B, int H,
+                                  int H_kv, int D, int block_size, int num_blocks, float scale,
+                                  int q_dtype, int kv_dtype, int num_threads) {
+  if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks < 0 || !orc_dtype_ok(q_dtype) || !orc_dtype_ok(kv_dtype))
+    return ORC_ERR_ARG;
+  const int group = H / H_kv;
+  const double sc = (double)scale;
+  int status = ORC_OK;
+  const int64_t n_pairs = (int64_t)B * H_kv;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(max : status)
+  for (int64_t pair = 0; pair < n_pairs; ++pair) {
+    const int b = (int)(pair / H_kv);
+    const int hk = (int)(pair % H_kv);
+    const int L = context_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size) {
+      if (hk == 0) orc_fill_rows(out, b, H, D, NAN);
+      status = ORC_ERR_DATA;
+      continue;
+    }
+    if (L == 0) {
+      for (int j = 0; j < group; ++j)
+        for (int d = 0; d < D; ++d) out[((size_t)b * H + (size_t)hk * group + j) * D + d] = 0.0;
+      continue;
+    }
+    double* Kc = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    const int32_t* row = block_tables + (size_t)b * max_blocks;
+    if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
+                   kv_dtype) != 0) {
+      for (int j = 0; j < group; ++j)
+        for (int d = 0; d < D; ++d)
+          out[((size_t)b * H + (size_t)hk * group + j) * D + d] = NAN;
+      status = ORC_ERR_DATA;
+      free(Kc);
+      free(Vc);
+      free(s);
+      continue;
+    }
+    for (int j = 0; j < group; ++j) {
+      const int h = hk * group + j; /* query head h reads kv-head h / group == hk */
+      const size_t qoff = ((size_t)b * H + h) * (size_t)D;
+      double mx = -INFINITY;
+      for (int t = 0; t < L; ++t) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += orc_load(q, qoff + d, q_dtype) * Kc[(size_t)t * D + d];
+        s[t] = sc * dot;
+        if (s[t] > mx) mx = s[t];
+      }
+      double den = 0.0;
+      for (int t = 0; t < L; ++t) den += exp(s[t] - mx);
+      double* o = out + qoff;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int t = 0; t < L; ++t) {
+        const double p = exp(s[t] - mx) / den;
+        for (int d = 0; d < D; ++d) o[d] += p * Vc[(size_t)t * D + d];
+      }
+    }
+    free(Kc);
+    free(Vc);
+    free(s);
+  }
+  return status;
+}
+
+/*
+ * Unnormalised attention of query head h of request b over tokens [t0, t1):
+ *   m = max_t s_t,  l = sum_t exp(s_t - m),  o = sum_t exp(s_t - m) V_t.
+ * This is the per-piece state of a sequence split; it is here only to show, in a test,
+ * that merging pieces gives back the plain definition above.
+ */
+int oracle_attention_partial(double* m_out, double* l_out, double* o_out, const void* q,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks, int b, int h, int t0,
+                             int t1, int H, int H_kv, int D, int block_size, int num_blocks,
+                             float scale, int q_dtype, int kv_dtype) {
+  if (t0 < 0 || t1 <= t0 || H % H_kv != 0 || !orc_dtype_ok(q_dtype) || !orc_dtype_ok(kv_dtype))
+    return ORC_ERR_ARG;
+  const int hk = h / (H / H_kv);
+  const int L = t1;
+  double* Kc = (double*)malloc(sizeof(double) * (size_t)L * D);
+  double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
+  const int32_t* row = block_tables + (size_t)b * max_blocks;
+  if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
+                 kv_dtype) != 0) {
+    free(Kc);
+    free(Vc);
+    return ORC_ERR_DATA;
+  }
+  const size_t qoff = ((size_t)b * H + h) * (size_t)D;
+  double mx = -INFINITY;
+  double* s = (double*)malloc(sizeof(double) * (size_t)L);
+  for (int t = t0; t < t1; ++t) {
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += orc_load(q, qoff + d, q_dtype) * Kc[(size_t)t * D + d];
+    s[t] = (double)scale * dot;
+    if (s[t] > mx) mx = s[t];
+  }
+  double l = 0.0;
+  for (int d = 0; d < D; ++d) o_out[d] = 0.0;
+  for (int t = t0; t < t1; ++t) {
+    const double w = exp(s[t] - mx);
+    l += w;
+    for (int d = 0; d < D; ++d) o_out[d] += w * Vc[(size_t)t * D + d];
+  }
+  *m_out = mx;
+  *l_out = l;
+  free(Kc);
+  free(Vc);
+  free(s);
+  return ORC_OK;
+}
+
+/*
+ * Log-sum-exp merge of n pieces (m_j, l_j, o_j[D]):
+ *   M = max_j m_j,  L = sum_j l_j exp(m_j - M),  out = sum_j o_j exp(m_j - M) / L.
+ */
+int oracle_lse_combine(int n, const double* m, const double* l, const double* o, int D,
+                       double* out) {
+  if (n <= 0 || D <= 0) return ORC_ERR_ARG;
+  double M = -INFINITY;
+  for (int j = 0; j < n; ++j)
+    if (m[j] > M) M = m[j];
+  double Lsum = 0.0;
+  for (int j = 0; j < n; ++j) Lsum += l[j] * exp(m[j] - M);
+  for (int d = 0; d < D; ++d) {
+    double acc = 0.0;
+    for (int j = 0; j < n; ++j) acc += o[(size_t)j * D + d] * exp(m[j] - M);
+    out[d] = acc / Lsum;
+  }
+  return ORC_OK;
+}

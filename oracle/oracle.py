@@ -1,0 +1,151 @@
+"""ctypes front end of the fp64 CPU oracle in ``oracle.c``.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` use this module. It imports nothing from the CUDA library and the CUDA
+library imports nothing from it.
+
+Arrays are NumPy arrays. A bf16 tensor is passed as its raw bits in a ``uint16`` array;
+an fp32 tensor as ``float32``. What each function computes, and the page sections it
+follows, is stated in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+ORC_F32, ORC_BF16 = 0, 1
+ORC_OK, ORC_ERR_ARG, ORC_ERR_DATA = 0, 1, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile ``oracle.c`` into a shared library with gcc (OpenMP, -O2)."""
+    stale = (not os.path.exists(out)) or os.path.getmtime(out) < os.path.getmtime(src)
+    if force or stale:
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library and declare its signatures."""
+    global _lib
+    with _lock:
+        if path is None and _lib is not None:
+            return _lib
+        lib_path = path or build()
+        lib = ctypes.CDLL(lib_path)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.oracle_version.restype = I
+        lib.oracle_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_kv_append.restype = I
+        lib.oracle_kv_pack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_kv_pack_blocks.restype = I
+        lib.oracle_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F,
+                                                      I, I, I]
+        lib.oracle_paged_decode_attention.restype = I
+        lib.oracle_attention_partial.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
+                                                 I, F, I, I]
+        lib.oracle_attention_partial.restype = I
+        lib.oracle_lse_combine.argtypes = [I, P, P, P, I, P]
+        lib.oracle_lse_combine.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return ORC_F32
+    if a.dtype == np.uint16:
+        return ORC_BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits) arrays, got {a.dtype}")
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, lib=None) -> int:
+    """In-place append of one token per request into the caches; returns the status."""
+    lib = lib or load()
+    NB, bs, H_kv, D = k_cache.shape
+    B = slot_mapping.shape[0]
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    return lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(slot_mapping), B, H_kv, D, bs, NB, _dtype_code(k_cache))
+
+
+def kv_pack_blocks(k_cache, v_cache, block_table_row, context_len: int, lib=None):
+    """Gather one request's K/V into a dense ``[L, 2, H_kv, D]`` array; returns (out, status)."""
+    lib = lib or load()
+    NB, bs, H_kv, D = k_cache.shape
+    out = np.zeros((context_len, 2, H_kv, D), dtype=k_cache.dtype)
+    row = np.ascontiguousarray(block_table_row, dtype=np.int32)
+    st = lib.oracle_kv_pack_blocks(_ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(row),
+                                   int(context_len), H_kv, D, bs, NB, _dtype_code(k_cache))
+    return out, st
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           num_threads: int = 0, lib=None):
+    """fp64 decode attention over the paged cache; returns (out[B,H,D] float64, status)."""
+    lib = lib or load()
+    B, H, D = q.shape
+    NB, bs, H_kv, D2 = k_cache.shape
+    assert D == D2 and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    max_blocks = bt.shape[1] if bt.ndim == 2 else 0
+    out = np.zeros((B, H, D), dtype=np.float64)
+    st = lib.oracle_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), max_blocks, _ptr(cl), B, H,
+        H_kv, D, bs, NB, ctypes.c_float(scale), _dtype_code(q), _dtype_code(k_cache),
+        int(num_threads))
+    return out, st
+
+
+def attention_partial(q, k_cache, v_cache, block_tables, b: int, h: int, t0: int, t1: int,
+                      scale: float, lib=None):
+    """Unnormalised (m, l, o) of head h of request b over tokens [t0, t1)."""
+    lib = lib or load()
+    B, H, D = q.shape
+    NB, bs, H_kv, _ = k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    m = np.zeros(1, np.float64)
+    l_ = np.zeros(1, np.float64)
+    o = np.zeros(D, np.float64)
+    st = lib.oracle_attention_partial(_ptr(m), _ptr(l_), _ptr(o), _ptr(q), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(bt), bt.shape[1], b, h, t0, t1, H,
+                                      H_kv, D, bs, NB, ctypes.c_float(scale), _dtype_code(q),
+                                      _dtype_code(k_cache))
+    if st != ORC_OK:
+        raise RuntimeError(f"oracle_attention_partial failed with status {st}")
+    return float(m[0]), float(l_[0]), o
+
+
+def lse_combine(m, l_, o, lib=None):
+    """Log-sum-exp merge of pieces m[n], l[n], o[n, D] into one normalised row."""
+    lib = lib or load()
+    m = np.ascontiguousarray(m, np.float64)
+    l_ = np.ascontiguousarray(l_, np.float64)
+    o = np.ascontiguousarray(o, np.float64)
+    n, D = o.shape
+    out = np.zeros(D, np.float64)
+    st = lib.oracle_lse_combine(n, _ptr(m), _ptr(l_), _ptr(o), D, _ptr(out))
+    if st != ORC_OK:
+        raise RuntimeError(f"oracle_lse_combine failed with status {st}")
+    return out

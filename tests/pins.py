@@ -1,0 +1,287 @@
+"""Pins of the fp64 oracle to facts other than itself.
+
+Each ``pin_*`` function takes an oracle library handle and raises ``AssertionError`` when
+the oracle disagrees with what the pages or the mathematics fix. ``test_oracle_pins.py``
+runs them on the real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle
+with one planted mistake each and checks that some pin fails.
+
+Facts used:
+  - hand-derived closed forms stored under ``tests/golden/``;
+  - a context of one token returns that token's V exactly;
+  - identical keys (or scale 0) give the mean of V; one dominant key gives its V;
+  - permuting physical blocks and rewriting the tables leaves the output bit-identical
+    (PagedAttention: blocks need not be contiguous, page "From PagedAttention to
+    Prefill-Decode disaggregation", sec. 2.2 step 2);
+  - two requests mapped to the same blocks with the same q give identical rows
+    (shared prefixes, same page, sec. 2.3);
+  - a dense, unpaged NumPy attention over the contiguous history agrees to 1e-12;
+  - GQA equals MHA with each kv-head replicated;
+  - the log-sum-exp merge of pieces equals the whole;
+  - output is linear in V;
+  - append then pack gives back the history plus the new token, bit for bit.
+"""
+from __future__ import annotations
+
+import glob
+import json
+import math
+import os
+
+import numpy as np
+
+from oracle import brute
+from oracle import oracle as orc
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- input construction
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round binary32 values to bf16 (round to nearest, ties to even); return the bits."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def as_stored(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_bf16_bits(x) if dtype == "bf16" else np.ascontiguousarray(x, np.float32)
+
+
+def stored_to_f64(a: np.ndarray) -> np.ndarray:
+    return brute.bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+class Paged:
+    """Contiguous per-request histories scattered into a paged pool by a random permutation."""
+
+    def __init__(self, rng, lengths, H, H_kv, D, bs, dtype="f32", spare_blocks=3, q=None,
+                 hist=None):
+        self.lengths = np.asarray(lengths, np.int32)
+        B = len(lengths)
+        self.B, self.H, self.H_kv, self.D, self.bs, self.dtype = B, H, H_kv, D, bs, dtype
+        nblk = [(int(L) + bs - 1) // bs for L in lengths]
+        self.NB = sum(nblk) + spare_blocks
+        self.max_blocks = max(1, max(nblk) if nblk else 1)
+        self.q = as_stored(rng.standard_normal((B, H, D)) if q is None else q, dtype)
+        if hist is None:
+            hist = [(rng.standard_normal((int(L), H_kv, D)), rng.standard_normal((int(L), H_kv, D)))
+                    for L in lengths]
+        self.K = [as_stored(k, dtype) for k, _ in hist]
+        self.V = [as_stored(v, dtype) for _, v in hist]
+        # pool filled with unrelated values, so a wrong read changes the answer
+        self.k_cache = as_stored(rng.standard_normal((self.NB, bs, H_kv, D)) * 7.0, dtype)
+        self.v_cache = as_stored(rng.standard_normal((self.NB, bs, H_kv, D)) * 7.0, dtype)
+        perm = rng.permutation(self.NB).astype(np.int32)
+        self.bt = np.full((B, self.max_blocks), -1, np.int32)
+        off = 0
+        for b, L in enumerate(lengths):
+            n = nblk[b]
+            self.bt[b, :n] = perm[off:off + n]
+            off += n
+            for t in range(int(L)):
+                blk, row = self.bt[b, t // bs], t % bs
+                self.k_cache[blk, row] = self.K[b][t]
+                self.v_cache[blk, row] = self.V[b][t]
+
+    def oracle(self, lib, scale):
+        return orc.paged_decode_attention(self.q, self.k_cache, self.v_cache, self.bt,
+                                          self.lengths, scale, lib=lib)
+
+    def dense(self, scale):
+        return np.stack([brute.dense_decode_attention(stored_to_f64(self.q[b]),
+                                                      stored_to_f64(self.K[b]),
+                                                      stored_to_f64(self.V[b]), scale)
+                         for b in range(self.B)])
+
+
+# ---------------------------------------------------------------- pins
+def pin_golden(lib):
+    files = sorted(glob.glob(os.path.join(GOLDEN_DIR, "*closed_form*.json")))
+    assert files, "no golden fixtures"
+    for path in files:
+        g = json.load(open(path))
+        q = np.array(g["q"], np.float32)
+        kc = np.array(g["k_cache"], np.float32)
+        vc = np.array(g["v_cache"], np.float32)
+        out, st = orc.paged_decode_attention(q, kc, vc, np.array(g["block_tables"], np.int32),
+                                             np.array(g["context_lens"], np.int32), g["scale"],
+                                             lib=lib)
+        assert st == orc.ORC_OK, (path, st)
+        err = np.abs(out - np.array(g["expected"])).max()
+        assert err <= g["tolerance"], (os.path.basename(path), err)
+
+
+def pin_ctx1_returns_v(lib):
+    rng = np.random.default_rng(11)
+    for dtype in ("f32", "bf16"):
+        p = Paged(rng, [1, 1, 1], H=4, H_kv=2, D=16, bs=4, dtype=dtype)
+        out, st = p.oracle(lib, 0.25)
+        assert st == orc.ORC_OK
+        for b in range(p.B):
+            for h in range(p.H):
+                want = stored_to_f64(p.V[b][0, h // 2])
+                assert np.array_equal(out[b, h], want), (dtype, b, h)
+
+
+def pin_identical_keys_mean(lib):
+    rng = np.random.default_rng(12)
+    L, H_kv, D = 37, 2, 8
+    k1 = rng.standard_normal((1, H_kv, D))
+    hist = [(np.repeat(k1, L, axis=0), rng.standard_normal((L, H_kv, D)))]
+    p = Paged(rng, [L], H=2, H_kv=H_kv, D=D, bs=8, hist=hist)
+    out, st = p.oracle(lib, 0.7)
+    assert st == orc.ORC_OK
+    want = stored_to_f64(p.V[0]).mean(axis=0)
+    assert np.abs(out[0] - want).max() <= 1e-12
+
+
+def pin_scale_zero_mean_and_dominant_key(lib):
+    rng = np.random.default_rng(13)
+    L, D = 21, 8
+    p = Paged(rng, [L], H=1, H_kv=1, D=D, bs=4)
+    out, st = p.oracle(lib, 0.0)
+    assert st == orc.ORC_OK
+    assert np.abs(out[0, 0] - stored_to_f64(p.V[0])[:, 0].mean(axis=0)).max() <= 1e-12
+    # one key aligned with q and a large scale: its weight dominates by e^(scale*gap)
+    K = np.zeros((L, 1, D))
+    K[9, 0, 0] = 1.0
+    q = np.zeros((1, 1, D))
+    q[0, 0, 0] = 1.0
+    hist = [(K, rng.standard_normal((L, 1, D)))]
+    p = Paged(rng, [L], H=1, H_kv=1, D=D, bs=4, q=q, hist=hist)
+    out, st = p.oracle(lib, 2000.0)  # exp(2000) overflows unless the max is subtracted
+    assert st == orc.ORC_OK
+    assert np.all(np.isfinite(out))
+    assert np.abs(out[0, 0] - stored_to_f64(p.V[0])[9, 0]).max() <= 1e-12
+
+
+def pin_block_permutation_invariance(lib):
+    rng = np.random.default_rng(14)
+    for dtype in ("f32", "bf16"):
+        p = Paged(rng, [5, 16, 17, 40], H=4, H_kv=2, D=8, bs=4, dtype=dtype)
+        out1, _ = p.oracle(lib, 0.3)
+        perm = rng.permutation(p.NB)
+        inv = np.argsort(perm)
+        k2 = np.ascontiguousarray(p.k_cache[perm])
+        v2 = np.ascontiguousarray(p.v_cache[perm])
+        bt2 = np.where(p.bt >= 0, inv[np.maximum(p.bt, 0)], -1).astype(np.int32)
+        out2, _ = orc.paged_decode_attention(p.q, k2, v2, bt2, p.lengths, 0.3, lib=lib)
+        assert np.array_equal(out1, out2), dtype
+
+
+def pin_brute_force(lib):
+    rng = np.random.default_rng(15)
+    cases = [([1, 17, 33, 100], 2, 2, 64, 16, "f32"),
+             ([3, 8, 9, 0, 25], 4, 1, 16, 8, "bf16"),
+             ([31, 2, 64], 8, 2, 32, 16, "bf16"),
+             ([7, 19], 6, 3, 8, 4, "f32")]
+    for lengths, H, H_kv, D, bs, dtype in cases:
+        p = Paged(rng, lengths, H=H, H_kv=H_kv, D=D, bs=bs, dtype=dtype)
+        scale = float(np.float32(1.0 / math.sqrt(D)))
+        out, st = p.oracle(lib, scale)
+        assert st == orc.ORC_OK
+        ref = p.dense(scale)
+        assert np.abs(out - ref).max() <= 1e-12, (lengths, H, H_kv, D, bs, dtype)
+
+
+def pin_shared_prefix_rows(lib):
+    rng = np.random.default_rng(16)
+    p = Paged(rng, [24, 9], H=2, H_kv=1, D=8, bs=4)
+    q = p.q.copy()
+    q[1] = q[0]
+    bt = p.bt.copy()
+    bt[1] = bt[0]  # request 1 maps to request 0's blocks
+    lens = np.array([24, 24], np.int32)
+    out, st = orc.paged_decode_attention(q, p.k_cache, p.v_cache, bt, lens, 0.5, lib=lib)
+    assert st == orc.ORC_OK
+    assert np.array_equal(out[0], out[1])
+
+
+def pin_gqa_equals_replicated_mha(lib):
+    rng = np.random.default_rng(17)
+    H, H_kv, D, bs = 8, 2, 16, 4
+    p = Paged(rng, [13, 30], H=H, H_kv=H_kv, D=D, bs=bs)
+    out_gqa, _ = p.oracle(lib, 0.25)
+    g = H // H_kv
+    k_rep = np.ascontiguousarray(np.repeat(p.k_cache, g, axis=2))
+    v_rep = np.ascontiguousarray(np.repeat(p.v_cache, g, axis=2))
+    out_mha, _ = orc.paged_decode_attention(p.q, k_rep, v_rep, p.bt, p.lengths, 0.25, lib=lib)
+    assert np.abs(out_gqa - out_mha).max() <= 1e-13
+
+
+def pin_split_merge_equals_whole(lib):
+    rng = np.random.default_rng(18)
+    p = Paged(rng, [50], H=2, H_kv=1, D=8, bs=4)
+    whole, _ = p.oracle(lib, 0.4)
+    for cuts in ([0, 50], [0, 16, 50], [0, 1, 2, 49, 50], [0, 20, 21, 36, 50]):
+        for h in range(2):
+            pieces = [orc.attention_partial(p.q, p.k_cache, p.v_cache, p.bt, 0, h, a, b, 0.4,
+                                            lib=lib) for a, b in zip(cuts[:-1], cuts[1:])]
+            m = [x[0] for x in pieces]
+            l_ = [x[1] for x in pieces]
+            o = np.stack([x[2] for x in pieces])
+            merged = orc.lse_combine(m, l_, o, lib=lib)
+            assert np.abs(merged - whole[0, h]).max() <= 1e-13, (cuts, h)
+
+
+def pin_linear_in_v(lib):
+    rng = np.random.default_rng(19)
+    L, H_kv, D = 23, 1, 8
+    K = rng.standard_normal((L, H_kv, D))
+    # small integers, so V1 + V2 is exact in binary32 and linearity is exact up to fp64 rounding
+    V1 = rng.integers(-8, 9, (L, H_kv, D)).astype(np.float64)
+    V2 = rng.integers(-8, 9, (L, H_kv, D)).astype(np.float64)
+    q = rng.standard_normal((1, 1, D))
+    outs = []
+    for V in (V1, V2, V1 + V2):
+        p = Paged(np.random.default_rng(5), [L], H=1, H_kv=1, D=D, bs=4, q=q, hist=[(K, V)])
+        outs.append(p.oracle(lib, 0.5)[0])
+    assert np.abs(outs[0] + outs[1] - outs[2]).max() <= 1e-12
+
+
+def pin_error_rows(lib):
+    rng = np.random.default_rng(20)
+    p = Paged(rng, [5, 9, 0], H=2, H_kv=1, D=4, bs=4)
+    out, st = p.oracle(lib, 0.5)
+    assert st == orc.ORC_OK
+    assert np.all(out[2] == 0.0)  # empty history: zero row
+    bt = p.bt.copy()
+    bt[1, 1] = p.NB + 5  # block id out of range
+    out, st = orc.paged_decode_attention(p.q, p.k_cache, p.v_cache, bt, p.lengths, 0.5, lib=lib)
+    assert st == orc.ORC_ERR_DATA and np.all(np.isnan(out[1])) and np.all(np.isfinite(out[0]))
+    lens = p.lengths.copy()
+    lens[0] = p.max_blocks * p.bs + 1  # longer than the table can hold
+    out, st = orc.paged_decode_attention(p.q, p.k_cache, p.v_cache, p.bt, lens, 0.5, lib=lib)
+    assert st == orc.ORC_ERR_DATA and np.all(np.isnan(out[0])) and np.all(np.isfinite(out[1]))
+
+
+def pin_append_then_pack_roundtrip(lib):
+    rng = np.random.default_rng(21)
+    for dtype in ("f32", "bf16"):
+        H_kv, D, bs = 2, 8, 4
+        hist_len = [4, 6, 11]
+        p = Paged(rng, [L + 1 for L in hist_len], H=2, H_kv=H_kv, D=D, bs=bs, dtype=dtype)
+        # the last position of each request is a fresh slot: overwrite it with garbage first
+        new_k = as_stored(rng.standard_normal((3, H_kv, D)), dtype)
+        new_v = as_stored(rng.standard_normal((3, H_kv, D)), dtype)
+        slots = np.zeros(3, np.int32)
+        for b, L in enumerate(hist_len):
+            blk, row = p.bt[b, L // bs], L % bs
+            slots[b] = blk * bs + row
+            p.k_cache[blk, row] = as_stored(np.full((H_kv, D), 99.0), dtype)
+            p.v_cache[blk, row] = as_stored(np.full((H_kv, D), -99.0), dtype)
+        slots_pad = np.concatenate([slots, [-1]]).astype(np.int32)  # -1 is padding
+        nk = np.concatenate([new_k, new_k[:1]])
+        nv = np.concatenate([new_v, new_v[:1]])
+        st = orc.kv_append(nk, nv, p.k_cache, p.v_cache, slots_pad, lib=lib)
+        assert st == orc.ORC_OK
+        for b, L in enumerate(hist_len):
+            packed, st = orc.kv_pack_blocks(p.k_cache, p.v_cache, p.bt[b], L + 1, lib=lib)
+            assert st == orc.ORC_OK
+            want = np.stack([np.concatenate([p.K[b][:L], new_k[b:b + 1]]),
+                             np.concatenate([p.V[b][:L], new_v[b:b + 1]])], axis=1)
+            assert packed.dtype == want.dtype
+            assert np.array_equal(packed.view(np.uint8), want.view(np.uint8)), (dtype, b)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,80 @@
+"""Each planted mistake in a copy of the oracle must make at least one pin fail.
+
+The mistakes are the plausible ones: a wrong row or head index, a dropped scale, a
+softmax without the max subtraction or with the wrong sign, P multiplied into K instead
+of V, the last token dropped, a combine that forgets the piece weights, an append or pack
+that writes the wrong place, and a wrong bf16 upcast. The copies are compiled on the CPU
+into a temporary folder; the real oracle is untouched.
+"""
+import os
+
+import pytest
+
+import pins
+from oracle import oracle as orc
+
+SRC = os.path.join(os.path.dirname(orc.__file__), "oracle.c")
+
+# (name, [(old, new, occurrence index or None for all)])
+MUTANTS = [
+    ("gqa_strided_grouping",
+     [("const int h = hk * group + j;", "const int h = j * H_kv + hk;", None)]),
+    ("wrong_row_in_block",
+     [("(size_t)(t % block_size);\n    const size_t base",
+       "(size_t)((t + 1) % block_size);\n    const size_t base", None)]),
+    ("scale_dropped", [("s[t] = sc * dot;", "s[t] = dot;", None)]),
+    ("no_max_subtraction",
+     [("den += exp(s[t] - mx);", "den += exp(s[t]);", None),
+      ("const double p = exp(s[t] - mx) / den;", "const double p = exp(s[t]) / den;", None)]),
+    ("softmax_sign_flipped",
+     [("den += exp(s[t] - mx);", "den += exp(mx - s[t]);", None),
+      ("const double p = exp(s[t] - mx) / den;", "const double p = exp(mx - s[t]) / den;", None)]),
+    ("pv_reads_k", [("o[d] += p * Vc[(size_t)t * D + d];", "o[d] += p * Kc[(size_t)t * D + d];",
+                     None)]),
+    ("last_token_dropped",
+     [("const int L = context_lens[b];",
+       "const int L = context_lens[b] > 1 ? context_lens[b] - 1 : context_lens[b];", None)]),
+    ("query_head_uses_kv_head_index",
+     [("const size_t qoff = ((size_t)b * H + h) * (size_t)D;\n      double mx",
+       "const size_t qoff = ((size_t)b * H + hk) * (size_t)D;\n      double mx", None)]),
+    ("append_wrong_offset",
+     [("(size_t)block * (size_t)block_size + (size_t)offset)",
+       "(size_t)block * (size_t)block_size + (size_t)((offset + 1) % block_size))", None)]),
+    ("pack_swaps_k_and_v",
+     [("memcpy(dst, (const char*)k_cache + src, row_bytes);",
+       "memcpy(dst, (const char*)v_cache + src, row_bytes);", None),
+      ("memcpy(dst + row_bytes, (const char*)v_cache + src, row_bytes);",
+       "memcpy(dst + row_bytes, (const char*)k_cache + src, row_bytes);", None)]),
+    ("bf16_upcast_shift", [("((uint32_t)h) << 16", "((uint32_t)h) << 15", None)]),
+    ("combine_forgets_weights", [("Lsum += l[j] * exp(m[j] - M);", "Lsum += l[j];", None)]),
+]
+
+
+def _mutate(text, edits):
+    for old, new, occ in edits:
+        n = text.count(old)
+        assert n >= 1, f"mutation anchor not found: {old!r}"
+        if occ is None:
+            text = text.replace(old, new)
+        else:
+            parts = text.split(old)
+            text = old.join(parts[: occ + 1]) + new + old.join(parts[occ + 1:])
+    return text
+
+
+@pytest.mark.parametrize("name,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, edits):
+    src = open(SRC).read()
+    mutated = _mutate(src, edits)
+    assert mutated != src
+    msrc = tmp_path / f"oracle_{name}.c"
+    msrc.write_text(mutated)
+    lib_path = orc.build(force=True, src=str(msrc), out=str(tmp_path / f"lib_{name}.so"))
+    lib = orc.load(lib_path)
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches the mutant {name}"
