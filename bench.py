@@ -1,0 +1,515 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step over a paged KV cache on GB300.
+
+A step is the whole hot path on one batch: ``kv_append`` of each request's new token,
+``paged_decode_attention`` (partial kernel + log-sum-exp combine) over every request's
+history, and ``kv_pack_blocks`` of the longest requests into contiguous transfer buffers.
+The default workload is ``gqa_skew_b256`` (B=256, H=32, H_kv=8, D=128, bf16, context
+log-uniform in [16, 32768], pack of the 8 longest), the largest of the five synthetic
+workloads and the only one that exercises every step.
+
+Prints one JSON line. ``value`` is algorithmic GB/s of the step (bytes every kernel must
+move at least once, see ``step_bytes``) over the device time of the step, inputs resident
+in HBM, L2 flushed between steps. ``e2e`` is the same metric with the step's inputs copied
+from pinned host memory and its outputs copied back inside the timed region.
+``roofline`` reports the attention call against the measured HBM copy bandwidth.
+``cpu_baseline`` is the fp64 CPU oracle timed on a bounded sample of the same workload.
+``--impl reference`` times only that oracle (the CPU reference arm).
+
+Multi-GPU: every rank runs an independent replica of the workload (requests shard with no
+exchange), so ``value`` is the sum over ranks and ``scaling`` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import shutil
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "gqa_skew_b256"
+METRIC = "paged decode-attn HBM GB/s (% of GB300 peak) and decode tokens/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SOURCES = ["paged_decode_attention_02_gb300/csrc/decode_attention.cu",
+                "paged_decode_attention_02_gb300/csrc/pda_device.cuh"]
+
+
+# ------------------------------------------------------------------ bytes
+def step_bytes(s, pack_reqs) -> dict:
+    """Algorithmic bytes: each element the op must read or write, once.
+
+    attention: K and V of every history token and kv-head (once, even under GQA), q and
+    out, the block-table entries in use and the context lengths. Workspace traffic, the
+    unused tail of each last block and unused pool blocks are not counted.
+    append: the new K/V read and written, plus the slot ids.
+    pack: the packed requests' K/V read and written, plus their table entries.
+    """
+    w = s.w
+    e = w.elem_bytes
+    L = s.context_lens_np.astype(np.int64)
+    bs = w.block_size
+    nblk = (L + bs - 1) // bs
+    kv_tok = 2 * w.H_kv * w.D * e
+    attn = int(L.sum()) * kv_tok + 2 * s.B * w.H * w.D * e + int(nblk.sum()) * 4 + s.B * 4
+    append = 2 * s.B * 2 * w.H_kv * w.D * e + s.B * 4
+    pl = np.array([int(L[r]) for r in pack_reqs], np.int64)
+    pack = int(pl.sum()) * kv_tok * 2 + int(((pl + bs - 1) // bs).sum()) * 4
+    return {"attention": attn, "append": append, "pack": pack,
+            "step": attn + append + pack, "tokens": int(L.sum())}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_partial_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_sha():
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            self.proc = subprocess.Popen(
+                [exe, f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def dist_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def _np(t):
+    import torch
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def oracle_pass(s, threads: int):
+    """One oracle pass over a step on host arrays: append, attention, pack. Returns seconds."""
+    from oracle import oracle as orc
+    kc, vc = _np(s.k_cache).copy(), _np(s.v_cache).copy()
+    q, kn, vn = _np(s.q), _np(s.k_new), _np(s.v_new)
+    t0 = time.perf_counter()
+    orc.kv_append(kn, vn, kc, vc, s.slot_mapping_np)
+    orc.paged_decode_attention(q, kc, vc, s.block_tables_np, s.context_lens_np, s.scale,
+                               num_threads=threads)
+    for r in s.pack_requests:
+        orc.kv_pack_blocks(kc, vc, s.block_tables_np[r], int(s.context_lens_np[r]))
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, seconds: float, threads: int):
+    """A step of workload w with as many requests as the oracle processes in ~`seconds`."""
+    from paged_decode_attention_02_gb300 import workloads as wl
+    probe_B = min(w.B, 8)
+    probe = wl.make_step(w, device="cpu", B=probe_B)
+    t = max(oracle_pass(probe, threads), 1e-3)
+    per_tok = t / max(1, int(probe.context_lens_np.sum()))
+    mean_tok = max(1.0, float(probe.context_lens_np.mean()))
+    B = int(min(w.B, max(probe_B, seconds / per_tok / mean_tok)))
+    return probe if B == probe_B else wl.make_step(w, device="cpu", B=B)
+
+
+def cpu_threads() -> int:
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import paged_decode_attention_02_gb300 as pda
+    from paged_decode_attention_02_gb300 import build_lib
+    from paged_decode_attention_02_gb300 import workloads as wl
+
+    build_lib.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.get(args.config)
+    s = wl.make_step(w, device=dev, B=args.batch)
+    pack_reqs = s.pack_requests
+    nb = step_bytes(s, pack_reqs)
+    stream = torch.cuda.current_stream(dev)
+
+    out = torch.empty_like(s.q)
+    cap = args.sm_cap
+    wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.torch_dtype, cap, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    packs = [torch.empty((int(s.context_lens_np[r]), 2, w.H_kv, w.D), dtype=w.torch_dtype,
+                         device=dev) for r in pack_reqs]
+    pack_rows = [s.block_tables[r] for r in pack_reqs]
+    pack_lens = [int(s.context_lens_np[r]) for r in pack_reqs]
+    launches_per_step = 1 + 2 + (1 if pack_reqs else 0)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+        if ev:
+            ev[1].record(stream)
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                   s.context_lens, s.max_context_len, s.scale, sm_cap=cap,
+                                   workspace=wsp, error_word=err)
+        if ev:
+            ev[2].record(stream)
+        if pack_reqs:
+            pda.kv_pack_blocks_batched(packs, s.k_cache, s.v_cache, pack_rows, pack_lens,
+                                       error_word=err)
+        if ev:
+            ev[3].record(stream)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            step(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        barrier(ws)
+    t_append = np.mean([e[0].elapsed_time(e[1]) for e in evs]) * 1e-3
+    t_attn = np.mean([e[1].elapsed_time(e[2]) for e in evs]) * 1e-3
+    t_pack = np.mean([e[2].elapsed_time(e[3]) for e in evs]) * 1e-3
+    t_step = np.mean([e[0].elapsed_time(e[3]) for e in evs]) * 1e-3
+    t_step_max = dist_max(t_step, ws)
+
+    # ---- end to end: per-step inputs from pinned host memory, results back to host
+    h_in = [x.detach().cpu().pin_memory() for x in
+            (s.q, s.k_new, s.v_new, s.slot_mapping, s.block_tables, s.context_lens)]
+    d_in = [s.q, s.k_new, s.v_new, s.slot_mapping, s.block_tables, s.context_lens]
+    h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory()] + [
+        torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in packs]
+    d_out = [out] + packs
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for d, h in zip(d_out, h_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        e2e_step()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_e2e = dist_max(np.mean([a.elapsed_time(b) for a, b in e2e_ev]) * 1e-3, ws)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during timing")
+
+    peak, peak_src = hbm_peak()
+    attn_gbs = nb["attention"] / t_attn / 1e9
+    traffic = profiled_traffic(w.name) if (args.batch is None and cap == 0) else None
+    res = {
+        "metric": METRIC,
+        "value": round(ws * nb["step"] / t_step_max / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step_max * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": s.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
+                   "block_size": w.block_size, "kv_dtype": w.dtype,
+                   "context_tokens": nb["tokens"], "pack_requests": len(pack_reqs),
+                   "sm_cap": cap, "parallelism": f"replicas x{ws}",
+                   "l2": f"flushed between steps (zero {2 * l2 >> 20} MiB); "
+                         f"KV set {nb['attention'] / 1e9:.2f} GB > L2"},
+        "attention": {"us": round(t_attn * 1e6, 2), "GBps": round(attn_gbs, 1),
+                      "frac_of_peak": round(attn_gbs / peak, 4),
+                      "decode_tokens_per_s_per_layer": round(s.B / t_attn, 1),
+                      "bytes": nb["attention"]},
+        "append": {"us": round(t_append * 1e6, 2),
+                   "GBps": round(nb["append"] / t_append / 1e9, 2), "bytes": nb["append"]},
+        "pack": {"us": round(t_pack * 1e6, 2),
+                 "GBps": round(nb["pack"] / t_pack / 1e9, 1) if t_pack > 0 else None,
+                 "bytes": nb["pack"]},
+        "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
+                     "traffic": traffic, "kernel": "paged_decode_attention call "
+                     "(attn_partial_kernel + attn_combine_kernel)", "peak_source": peak_src},
+        "e2e": {"value": round(ws * nb["step"] / t_e2e / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed": round(t_wall, 4),
+        "clocks": clk.summary(),
+    }
+
+    if args.sweeps and ws == 1:
+        res["workloads"] = sweep_workloads(args, dev, flush, peak)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        sample = oracle_sample(w, args.cpu_seconds, threads)
+        sb = step_bytes(sample, sample.pack_requests)
+        reps, t_cpu = 0, 0.0
+        while t_cpu < args.cpu_seconds * 0.5 or reps == 0:
+            t_cpu += oracle_pass(sample, threads)
+            reps += 1
+        res["cpu_baseline"] = {
+            "value": round(sb["step"] * reps / t_cpu / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{w.name} recipe with B={sample.B} ({sb['tokens']} tokens, pack of "
+                      f"{len(sample.pack_requests)}), fp64 C oracle, {reps} pass(es), "
+                      f"{t_cpu:.1f} s"}
+    return res
+
+
+def sweep_workloads(args, dev, flush, peak):
+    """Attention alone on the other full-size workloads, and the SM-fraction sweep."""
+    import torch
+
+    import paged_decode_attention_02_gb300 as pda
+    from paged_decode_attention_02_gb300 import workloads as wl
+
+    out_all = {}
+    sms = pda.device_sm_count()
+    stream = torch.cuda.current_stream(dev)
+    for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128"):
+        w = wl.get(name)
+        s = wl.make_step(w, device=dev)
+        nb = step_bytes(s, [])
+        caps = [0] + [int(math.ceil(p / 100 * sms)) for p in w.sm_caps_pct if p < 100]
+        res_w = {}
+        for cap in caps:
+            out = torch.empty_like(s.q)
+            wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.torch_dtype, cap,
+                                      dev)
+            for _ in range(3):
+                flush.zero_()
+                pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                           s.context_lens, s.max_context_len, s.scale,
+                                           sm_cap=cap, workspace=wsp)
+            ts = []
+            for _ in range(args.sweep_iters):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush.zero_()
+                a.record(stream)
+                pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                           s.context_lens, s.max_context_len, s.scale,
+                                           sm_cap=cap, workspace=wsp)
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            t = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e-3
+            gbs = nb["attention"] / t / 1e9
+            key = "all_sms" if cap == 0 else f"sm_cap_{cap}"
+            res_w[key] = {"us": round(t * 1e6, 2), "GBps": round(gbs, 1),
+                          "frac_of_peak": round(gbs / peak, 4),
+                          "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
+        res_w["bytes"] = nb["attention"]
+        out_all[name] = res_w
+        del s
+        torch.cuda.empty_cache()
+    return out_all
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, ws, rank):
+    """The fp64 CPU oracle on the host cores, on a bounded sample of the same workload."""
+    from paged_decode_attention_02_gb300 import workloads as wl
+
+    if rank != 0:
+        return None
+    w = wl.get(args.config)
+    threads = cpu_threads()
+    per_step = min(10.0, args.ref_budget_s / max(1, args.steps + args.warmup))
+    sample = oracle_sample(w, per_step, threads)
+    sb = step_bytes(sample, sample.pack_requests)
+    for _ in range(args.warmup):
+        oracle_pass(sample, threads)
+    times = [oracle_pass(sample, threads) for _ in range(args.steps)]
+    t = float(np.mean(times))
+    v = round(sb["step"] / t / 1e9, 4)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": sample.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
+                   "block_size": w.block_size, "kv_dtype": w.dtype,
+                   "context_tokens": sb["tokens"], "pack_requests": len(sample.pack_requests)},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{w.name} recipe with B={sample.B} of {w.B} requests "
+                                   f"({sb['tokens']} tokens) per step"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=HEADLINE, help="workload name or index (1-5)")
+    ap.add_argument("--batch", type=int, default=None, help="fewer requests (profiling only)")
+    ap.add_argument("--sm-cap", type=int, default=0, help="SMs the attention may use (0: all)")
+    ap.add_argument("--no-sweeps", dest="sweeps", action="store_false")
+    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

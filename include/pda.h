@@ -1,0 +1,189 @@
+/*
+ * pda.h -- C ABI of the paged decode-attention library for GB300 (sm_103a).
+ *
+ * The library implements the data-parallel hot path of one decode step over a paged KV
+ * cache: the append of each request's new K/V, the attention of each request's single
+ * query token over its whole cached history, and the gather of one request's scattered
+ * KV blocks into a contiguous buffer for transfer.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer unless its comment says "host". The caller
+ *    owns all memory; the library allocates nothing and keeps no per-call state.
+ *  - Tensors are dense and row-major with exactly the shapes given; no strides.
+ *  - KV caches are [num_blocks, block_size, H_kv, D]: physical block p holds block_size
+ *    consecutive tokens, token row r of block p is at ((p * block_size + r) * H_kv) * D.
+ *    (Page "From PagedAttention to Prefill-Decode disaggregation", sec. 2.2 step 1: the
+ *    cache is cut into fixed-size physical blocks, each holding the K and V of a fixed
+ *    number of tokens.)
+ *  - block_tables is [B, max_blocks_per_seq] int32: logical block i of request b is
+ *    physical block block_tables[b * max_blocks_per_seq + i]; blocks need not be
+ *    contiguous or ordered, and several requests may share blocks (same page, sec. 2.2
+ *    step 2 and sec. 2.3). Entries past a request's last block are never read.
+ *  - Query head h reads kv-head h / (H / H_kv) (grouped-query attention, contiguous groups).
+ *  - Every call is asynchronous on `stream`, never synchronises the host and makes no
+ *    allocation, so a sequence of calls can be captured in a CUDA graph once each kernel
+ *    has been launched at least once outside capture.
+ *  - Host-checkable errors (null pointers, bad sizes, unsupported dtypes or shapes,
+ *    misaligned pointers) return a status before anything is launched. Errors in device
+ *    data (a block id or slot out of range, a context length beyond capacity) cannot be
+ *    seen on the host without a sync; kernels OR a PDA_DEVERR_* bit into *error_word
+ *    (when error_word is not NULL) and never trap. The caller zeroes the error word and
+ *    reads it back whenever it chooses to synchronise.
+ */
+#ifndef PDA_H
+#define PDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PDA_OK = 0,
+  PDA_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size, misalignment */
+  PDA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+  PDA_ERR_CUDA = 3,        /* a CUDA runtime call failed; see cudaGetLastError */
+  PDA_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+} pda_status;
+
+typedef enum { PDA_F32 = 0, PDA_BF16 = 1 } pda_dtype;
+
+/* Bits OR-ed into *error_word by the kernels. */
+#define PDA_DEVERR_CONTEXT_LEN 0x1 /* context_lens[b] < 0, > max_context_len or > table capacity */
+#define PDA_DEVERR_BLOCK_ID 0x2    /* a block id needed by a request is outside [0, num_blocks) */
+#define PDA_DEVERR_SLOT 0x4        /* slot_mapping[b] >= num_blocks * block_size */
+#define PDA_DEVERR_TIMEOUT 0x8     /* a pipeline wait passed its time limit; results invalid */
+
+/* Most requests one batched pack call takes. */
+#define PDA_PACK_MAX_BATCH 64
+
+/* Human-readable name of a status. Never NULL. */
+const char* pda_status_string(pda_status status);
+
+/* ABI version of this library (incremented on incompatible change). */
+int pda_version(void);
+
+/* Number of SMs of the current device, written to *num_sms (host). */
+pda_status pda_device_sm_count(int* num_sms);
+
+/*
+ * pda_kv_append -- write each request's new token into the paged cache.
+ *
+ * Defined by the decode step of page "Disaggregated LLM Serving: from PD disaggregation to
+ * attention offload", sec. 1 (second list, item 2): every decode step reads the cached
+ * history and appends the new token's K/V; the slot comes from the block table (page "From
+ * PagedAttention to Prefill-Decode disaggregation", sec. 2.2 step 3: blocks are handed out
+ * as tokens arrive).
+ *
+ *  k_new, v_new   [B, H_kv, D] in kv_dtype: this step's K and V of each request.
+ *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype, updated in place.
+ *  slot_mapping   [B] int32: flat slot s = block * block_size + row for request b. s < 0
+ *                 means "no token" (padding) and is skipped; s >= num_blocks * block_size
+ *                 sets PDA_DEVERR_SLOT and is skipped.
+ *  The copy is bitwise. Two requests given the same slot race; the caller must not do so.
+ *  Requires H_kv * D * sizeof(kv_dtype) to be a multiple of 16 bytes and 16-byte aligned
+ *  pointers. B == 0 is a no-op.
+ */
+pda_status pda_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* slot_mapping, int B, int H_kv, int D, int block_size,
+                         int num_blocks, pda_dtype kv_dtype, int32_t* error_word,
+                         cudaStream_t stream);
+
+/*
+ * pda_attention_workspace_size -- bytes of device workspace pda_paged_decode_attention
+ * needs on the current device for these sizes. The bound does not depend on the context
+ * lengths. Written to *bytes (host).
+ */
+pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block_size,
+                                        pda_dtype kv_dtype, int sm_cap, size_t* bytes);
+
+/*
+ * pda_paged_decode_attention -- one query token per head attends over its request's whole
+ * cached history, read through the block table.
+ *
+ * Defined by: decode reads the request's whole KV history each step (page "Disaggregated
+ * LLM Serving", sec. 1, and sec. 6.1 on why this is memory-bound); the history lives in
+ * fixed-size blocks reached through a per-request table (page "From PagedAttention to
+ * Prefill-Decode disaggregation", sec. 2.2). For each request b and query head h with
+ * kv-head k = h / (H / H_kv) and L = context_lens[b]:
+ *      s_t = scale * q[b,h,:] . K_t[k,:],   t < L
+ *      out[b,h,:] = sum_t softmax(s)_t * V_t[k,:]
+ * The work is split per request and kv-head and, for long histories, along the sequence;
+ * the pieces are merged with a log-sum-exp combine (the per-request split and merge of
+ * Orca's iteration-level batching, page "Disaggregated LLM Serving", sec. 2.1, applied
+ * also along the sequence). Accumulation is fp32.
+ *
+ *  out            [B, H, D] in out_dtype (PDA_F32 or PDA_BF16).
+ *  q              [B, H, D] in q_dtype; q_dtype must equal kv_dtype.
+ *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype; read only.
+ *  block_tables   [B, max_blocks_per_seq] int32.
+ *  context_lens   [B] int32 (device): tokens of history including this step's token.
+ *                 L == 0 gives a zero row. L < 0, L > max_context_len or
+ *                 L > max_blocks_per_seq * block_size gives NaN rows and
+ *                 PDA_DEVERR_CONTEXT_LEN. A block id out of range gives NaN rows for
+ *                 that (request, kv-head group) and PDA_DEVERR_BLOCK_ID.
+ *  max_context_len host upper bound of context_lens (validation only).
+ *  scale          softmax scale, usually 1/sqrt(D).
+ *  sm_cap         0 runs on every SM; n > 0 confines the kernel to at most n SMs (one
+ *                 resident block per SM, a persistent grid walks the work). This models
+ *                 attention sharing the GPU with other work on a fraction of its SMs
+ *                 (review of "Injecting Adrenaline into LLM Serving", sec. 3.3).
+ *  workspace      device scratch of at least pda_attention_workspace_size(...) bytes,
+ *                 256-byte aligned; no initialisation needed; not shared by calls that
+ *                 may run concurrently.
+ *  Supported: D in {64, 128}, block_size == 16, H / H_kv in {1, 2, 4, 8}, B <= 8192,
+ *  kv_dtype in {PDA_F32, PDA_BF16}. Pointers 16-byte aligned.
+ */
+pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int max_context_len, int B, int H, int H_kv, int D,
+                                      int block_size, int num_blocks, float scale,
+                                      pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype,
+                                      int sm_cap, void* workspace, size_t workspace_bytes,
+                                      int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_pack_blocks -- gather one request's KV into one contiguous buffer.
+ *
+ * Defined by the request-level KV transfer of PD disaggregation (page on goodput and PD
+ * disaggregation, 0539edu.com, sec. 5.4: after prefill, a request's whole KV is sent in
+ * one transfer) over the paged layout above: for t < context_len,
+ *      out[t, 0, :, :] = K of token t,   out[t, 1, :, :] = V of token t,
+ * token t being row t % block_size of physical block block_table_row[t / block_size].
+ *
+ *  out            [context_len, 2, H_kv, D] in kv_dtype, dense.
+ *  block_table_row device pointer to the request's table row (int32).
+ *  context_len    host int, tokens to pack; 0 is a no-op.
+ *  A block id out of range sets PDA_DEVERR_BLOCK_ID and fills that token's output with
+ *  0xFF bytes (a NaN pattern). The copy is bitwise. Needs H_kv * D * sizeof(kv_dtype) to be
+ *  a multiple of 16 bytes and 16-byte aligned pointers.
+ */
+pda_status pda_kv_pack_blocks(void* out, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table_row, int context_len, int H_kv, int D,
+                              int block_size, int num_blocks, pda_dtype kv_dtype,
+                              int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_pack_blocks_batched -- pda_kv_pack_blocks for n requests in one launch.
+ *
+ *  outs, block_table_rows, context_lens: HOST arrays of n entries; outs[i] and
+ *  block_table_rows[i] are device pointers, context_lens[i] a host count. The arrays are
+ *  copied into the launch, so the caller may reuse them when the call returns.
+ *  n <= PDA_PACK_MAX_BATCH. Same semantics per request as pda_kv_pack_blocks.
+ */
+pda_status pda_kv_pack_blocks_batched(void* const* outs, const int32_t* const* block_table_rows,
+                                      const int32_t* context_lens, int n, const void* k_cache,
+                                      const void* v_cache, int H_kv, int D, int block_size,
+                                      int num_blocks, pda_dtype kv_dtype, int32_t* error_word,
+                                      cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDA_H */

@@ -1,1 +1,12 @@
-"""Decode attention over a paged KV cache for GB300 (sm_103a)."""
+"""Decode attention over a paged KV cache for GB300 (sm_103a).
+
+The computation lives in ``libpda.so`` (CUDA kernels behind the C ABI of ``include/pda.h``);
+``binding`` marshals torch tensors into it and ``workloads`` draws seeded synthetic inputs.
+"""
+from .binding import (PdaError, alloc_workspace, attention_workspace_size, device_sm_count,
+                      kv_append, kv_pack_blocks, kv_pack_blocks_batched, paged_decode_attention,
+                      status_string)
+
+__all__ = ["PdaError", "alloc_workspace", "attention_workspace_size", "device_sm_count",
+           "kv_append", "kv_pack_blocks", "kv_pack_blocks_batched", "paged_decode_attention",
+           "status_string"]

@@ -1,0 +1,185 @@
+"""Thin ctypes binding over ``libpda.so`` (declared in ``include/pda.h``).
+
+Argument marshalling only: shapes, dtypes and devices are read off torch tensors and
+passed as plain pointers and sizes; every step of the computation runs in the library's
+CUDA kernels. The library must be built (``build_lib.build()``); if it is missing or
+fails to load, every call raises, and nothing falls back to another implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build_lib
+
+PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE = range(5)
+PDA_F32, PDA_BF16 = 0, 1
+PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
+PDA_PACK_MAX_BATCH = 64
+
+EXPORTED = [
+    "pda_status_string", "pda_version", "pda_device_sm_count", "pda_kv_append",
+    "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
+    "pda_kv_pack_blocks_batched",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return build_lib.LIB_PATH
+
+
+def load():
+    """Load libpda.so and declare its C signatures. Raises if the library is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpda.so is not built ({path}); run build_lib.build() first")
+        lib = ctypes.CDLL(path)
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.pda_status_string.argtypes = [I]
+        lib.pda_status_string.restype = ctypes.c_char_p
+        lib.pda_version.restype = I
+        lib.pda_device_sm_count.argtypes = [ctypes.POINTER(I)]
+        lib.pda_device_sm_count.restype = I
+        lib.pda_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+        lib.pda_kv_append.restype = I
+        lib.pda_attention_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
+        lib.pda_attention_workspace_size.restype = I
+        lib.pda_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F,
+                                                   I, I, I, I, P, SZ, P, P]
+        lib.pda_paged_decode_attention.restype = I
+        lib.pda_kv_pack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
+        lib.pda_kv_pack_blocks.restype = I
+        lib.pda_kv_pack_blocks_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P, P]
+        lib.pda_kv_pack_blocks_batched.restype = I
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().pda_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != PDA_OK:
+        raise PdaError(status, what)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PDA_F32
+    if t.dtype == torch.bfloat16:
+        return PDA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def device_sm_count() -> int:
+    n = ctypes.c_int(0)
+    _check(load().pda_device_sm_count(ctypes.byref(n)), "pda_device_sm_count")
+    return n.value
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, error_word=None, stream=None):
+    """Scatter each request's new K/V (``[B, H_kv, D]``) into its cache slot."""
+    NB, bs, H_kv, D = k_cache.shape
+    B = slot_mapping.shape[0]
+    assert k_new.shape == (B, H_kv, D) and v_new.shape == (B, H_kv, D)
+    assert slot_mapping.dtype == torch.int32
+    _check(load().pda_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(slot_mapping), B, H_kv, D, bs, NB, _dtype(k_cache),
+                                _ptr(error_word), _stream(stream)), "pda_kv_append")
+
+
+def attention_workspace_size(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat16,
+                             sm_cap=0) -> int:
+    n = ctypes.c_size_t(0)
+    dt = PDA_BF16 if kv_dtype == torch.bfloat16 else PDA_F32
+    _check(load().pda_attention_workspace_size(B, H, H_kv, D, block_size, dt, sm_cap,
+                                               ctypes.byref(n)), "pda_attention_workspace_size")
+    return n.value
+
+
+def alloc_workspace(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat16, sm_cap=0,
+                    device=None) -> torch.Tensor:
+    n = attention_workspace_size(B, H, H_kv, D, block_size, kv_dtype, sm_cap)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len: int, scale: float, sm_cap: int = 0, workspace=None,
+                           error_word=None, stream=None):
+    """``out[b,h] = softmax(scale q[b,h] K^T) V`` over request b's paged history."""
+    B, H, D = q.shape
+    NB, bs, H_kv, D2 = k_cache.shape
+    assert D == D2 and v_cache.shape == k_cache.shape and out.shape == q.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    if workspace is None:
+        workspace = alloc_workspace(B, H, H_kv, D, bs, k_cache.dtype, sm_cap, q.device)
+    _check(load().pda_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
+        _ptr(context_lens), int(max_context_len), B, H, H_kv, D, bs, NB, float(scale),
+        _dtype(q), _dtype(k_cache), _dtype(out), int(sm_cap), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
+        "pda_paged_decode_attention")
+    return out
+
+
+def kv_pack_blocks(out, k_cache, v_cache, block_table_row, context_len: int, error_word=None,
+                   stream=None):
+    """Gather one request's K/V into ``out[context_len, 2, H_kv, D]``."""
+    NB, bs, H_kv, D = k_cache.shape
+    assert out.shape[0] >= context_len and tuple(out.shape[1:]) == (2, H_kv, D)
+    _check(load().pda_kv_pack_blocks(_ptr(out), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_table_row), int(context_len), H_kv, D, bs, NB,
+                                     _dtype(k_cache), _ptr(error_word), _stream(stream)),
+           "pda_kv_pack_blocks")
+    return out
+
+
+def kv_pack_blocks_batched(outs, k_cache, v_cache, block_table_rows, context_lens,
+                           error_word=None, stream=None):
+    """``kv_pack_blocks`` for several requests in one launch."""
+    NB, bs, H_kv, D = k_cache.shape
+    n = len(outs)
+    assert len(block_table_rows) == n and len(context_lens) == n
+    out_arr = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
+    for o in outs:
+        _ptr(o)
+    row_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(r).value for r in block_table_rows])
+    len_arr = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in context_lens])
+    _check(load().pda_kv_pack_blocks_batched(out_arr, row_arr, len_arr, n, _ptr(k_cache),
+                                             _ptr(v_cache), H_kv, D, bs, NB, _dtype(k_cache),
+                                             _ptr(error_word), _stream(stream)),
+           "pda_kv_pack_blocks_batched")
+    return outs

@@ -1,0 +1,769 @@
+// decode_attention.cu -- batched single-query attention over a paged KV cache, sm_103a.
+//
+// What it computes: for each request b and query head h (kv-head k = h / G, G = H / H_kv),
+//   out[b,h] = sum_t softmax_t(scale * q[b,h] . K_t[k]) V_t[k],  t < context_lens[b],
+// with token t in physical block block_tables[b][t / 16], row t % 16. Decode reads the
+// whole cached history each step (page "Disaggregated LLM Serving: from PD disaggregation
+// to attention offload", sec. 1 and sec. 6.1); the history is paged (page "From
+// PagedAttention to Prefill-Decode disaggregation", sec. 2.2).
+//
+// How (GB300 design):
+//  * Unit of work = one tile = one physical block (16 tokens) of one kv-head: 16 rows of
+//    D elements for K and for V. Tiles are numbered request-major, then kv-head, then
+//    block, so the tiles of one (request, kv-head) "segment" are consecutive.
+//  * The total tile count is split evenly over all warps of a persistent grid (one block
+//    per SM, at most sm_cap SMs). Each warp is an independent worker: it streams its tile
+//    range through its own ring of shared-memory stages filled by TMA (3-D tiled
+//    cp.async.bulk.tensor for the K and V rows, a 1-D bulk copy for the segment's q rows),
+//    each stage guarded by an mbarrier. There is no block-wide synchronisation in the loop.
+//  * The G query heads that share a kv-head are processed together, so each K/V byte is
+//    read from HBM once (GQA).
+//  * Scores use fp32 FMAs; the partial dot products of a lane group are summed with a
+//    shuffle reduce-scatter, which leaves each lane owning a few complete (head, token)
+//    scores. Softmax is online, in base 2 (q is pre-scaled by scale * log2 e).
+//  * A segment that lies wholly inside one worker's range is normalised and written
+//    directly. A segment cut by a range boundary leaves (m, l, o) pieces in the workspace
+//    (at most two per worker), merged by attn_combine_kernel with a log-sum-exp combine:
+//    the split and merge of Orca's iteration-level batching (page "Disaggregated LLM
+//    Serving", sec. 2.1), applied along the sequence.
+//  * No tensor cores: per kv-head and token this is G dot products of length D against
+//    2 * D * sizeof(elem) bytes, far below the tensor-core break-even.
+#include <math.h>
+
+#include <cmath>
+
+#include "pda_device.cuh"
+#include "pda_internal.h"
+
+namespace pda {
+
+constexpr int kBS = 16;             // tokens per physical block (box height of the TMA)
+constexpr int kMaxWarps = 8;        // warps (workers) per block
+constexpr int kMaxBatch = 8192;     // prefix table size bound (shared memory)
+constexpr int kSmemBudget = 226 * 1024;  // dynamic bytes; static shared memory sits on top
+constexpr int kMinResidentSmem = 116 * 1024;  // > half an SM: never two blocks per SM
+
+struct AttnParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_o;         // [2 * num_workers][G][D]
+  float* ws_ml;        // [2 * num_workers][G][2]
+  int32_t* ws_prefix;  // [B + 1] block prefix sums, for the combine kernel
+  int32_t* error_word;
+  int B, H, H_kv, num_blocks, max_blocks, max_context_len;
+  int out_bf16;
+  float scale_log2;
+  int num_workers;
+  int stages;
+  uint32_t stage_bytes;   // one stage: K tile, V tile, q slot
+  uint32_t prefix_bytes;  // shared bytes reserved for the prefix table
+};
+
+// Worker w owns tiles [tile_start(w), tile_start(w + 1)).
+__host__ __device__ __forceinline__ int tile_start(int w, int W, int NW) {
+  return static_cast<int>((static_cast<long long>(w) * W) / NW);
+}
+// The worker whose range holds tile t (the largest w with tile_start(w) <= t).
+__host__ __device__ __forceinline__ int tile_owner(int t, int W, int NW) {
+  return static_cast<int>(((static_cast<long long>(t) + 1) * NW - 1) / W);
+}
+
+// Reduce-scatter over the lanes of one row group: n values per lane, xor masks from
+// `mask` down to 1. While n > 1 each step keeps half of the values (the upper half on
+// lanes whose mask bit is set) and adds the partner's copy of that half; once one value
+// is left the remaining steps are plain butterflies.
+template <int n, int mask>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (mask == 0) {
+      return;
+    } else if constexpr (n > 1) {
+      const bool upper = (lane & mask) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float keep = upper ? v[i + n / 2] : v[i];
+        const float send = upper ? v[i] : v[i + n / 2];
+        v[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
+      }
+      ReduceScatter<n / 2, mask / 2>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(kFullMask, v[0], mask);
+      ReduceScatter<1, mask / 2>::run(v, lane);
+    }
+  }
+};
+
+template <typename KV, int D, int G>
+struct Geometry {
+  using E = Elem<KV>;
+  static constexpr int VEC = E::kVec;               // elements per lane per row (16 bytes)
+  static constexpr int LPR = D / VEC;               // lanes covering one row
+  static constexpr int RPW = 32 / LPR;              // rows a warp covers per step
+  static constexpr int TPL = kBS / RPW;             // token slots per lane per tile
+  static constexpr int N = G * TPL;                 // partial dots per lane per tile
+  static constexpr int C = N >= LPR ? N / LPR : 1;  // complete scores per lane
+  static constexpr int DUP = N >= LPR ? 1 : LPR / N;  // lanes holding the same score
+  static constexpr int LPH = N >= LPR ? LPR / G : LPR;  // lanes of a row group per head
+  static constexpr uint32_t TILE_BYTES = kBS * D * sizeof(KV);
+  static constexpr uint32_t Q_BYTES = G * D * sizeof(KV);
+  static_assert(32 % LPR == 0 && kBS % RPW == 0, "row geometry");
+  static_assert(LPR >= G, "one head per lane after the reduce-scatter");
+  static_assert(TILE_BYTES % 128 == 0 && Q_BYTES % 16 == 0, "smem alignment");
+};
+
+// Per-warp online-softmax state and tile arithmetic.
+template <typename KV, int D, int G>
+struct WarpAttn {
+  using Geo = Geometry<KV, D, G>;
+  using E = typename Geo::E;
+  static constexpr int VEC = Geo::VEC, LPR = Geo::LPR, RPW = Geo::RPW, TPL = Geo::TPL;
+  static constexpr int N = Geo::N, C = Geo::C, DUP = Geo::DUP, LPH = Geo::LPH;
+
+  int lane, rw, cl, idx0;
+  float qr[G][VEC];
+  float o[G][VEC];
+  float m_own;  // running max of this lane's head (log2 domain)
+  float l_own;  // this lane's share of the running sum of its head
+
+  __device__ __forceinline__ void init(int lane_) {
+    lane = lane_;
+    rw = lane / LPR;
+    cl = lane % LPR;
+    idx0 = (cl / DUP) * C;
+  }
+
+  __device__ __forceinline__ void reset(const KV* q_smem, float scale_log2) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float t[VEC];
+      E::load16(q_smem + j * D + cl * VEC, t);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        qr[j][e] = t[e] * scale_log2;
+        o[j][e] = 0.f;
+      }
+    }
+    m_own = -INFINITY;
+    l_own = 0.f;
+  }
+
+  template <bool kPartial>
+  __device__ __forceinline__ void tile(const KV* ks, const KV* vs, int n_valid) {
+    float part[N];
+#pragma unroll
+    for (int i = 0; i < TPL; ++i) {
+      const int t = rw + RPW * i;
+      float k[VEC];
+      E::load16(ks + t * D + cl * VEC, k);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float acc = qr[j][0] * k[0];
+#pragma unroll
+        for (int e = 1; e < VEC; ++e) acc = fmaf(qr[j][e], k[e], acc);
+        part[j * TPL + i] = acc;
+      }
+    }
+    ReduceScatter<N, LPR / 2>::run(part, lane);
+
+    // part[0..C) are now complete scores of (head idx/TPL, slot idx%TPL), idx = idx0 + r.
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      if (kPartial) {
+        const int t = rw + RPW * ((idx0 + r) % TPL);
+        if (t >= n_valid) part[r] = -INFINITY;
+      }
+      tmax = fmaxf(tmax, part[r]);
+    }
+#pragma unroll
+    for (int mask = LPH / 2; mask >= 1; mask >>= 1)
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, mask));
+#pragma unroll
+    for (int mask = LPR; mask < 32; mask <<= 1)
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, mask));
+
+    const float m_new = fmaxf(m_own, tmax);
+    const float alpha = ex2(m_own - m_new);
+    m_own = m_new;
+    float psum = 0.f;
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      part[r] = ex2(part[r] - m_new);
+      psum += part[r];
+    }
+    l_own = l_own * alpha + ((cl % DUP) == 0 ? psum : 0.f);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float a = (G == 1) ? alpha : __shfl_sync(kFullMask, alpha, j * LPH);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) o[j][e] *= a;
+    }
+
+#pragma unroll
+    for (int i = 0; i < TPL; ++i) {
+      const int t = rw + RPW * i;
+      float v[VEC];
+      E::load16(vs + t * D + cl * VEC, v);
+      if (kPartial && t >= n_valid) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[e] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int idx = j * TPL + i;
+        const int src = rw * LPR + (idx / C) * DUP;
+        const float p = __shfl_sync(kFullMask, part[idx % C], src);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[j][e] = fmaf(p, v[e], o[j][e]);
+      }
+    }
+  }
+
+  // Sums the state over lanes; afterwards lanes of row group 0 hold, for every head j,
+  // o[j] over their dims, and lj[j], mj[j] on every lane.
+  __device__ __forceinline__ void reduce(float* lj, float* mj) {
+    float l = l_own;
+#pragma unroll
+    for (int mask = LPH / 2; mask >= 1; mask >>= 1) l += __shfl_xor_sync(kFullMask, l, mask);
+#pragma unroll
+    for (int mask = LPR; mask < 32; mask <<= 1) l += __shfl_xor_sync(kFullMask, l, mask);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+#pragma unroll
+        for (int mask = LPR; mask < 32; mask <<= 1)
+          o[j][e] += __shfl_xor_sync(kFullMask, o[j][e], mask);
+      lj[j] = __shfl_sync(kFullMask, l, j * LPH);
+      mj[j] = __shfl_sync(kFullMask, m_own, j * LPH);
+    }
+  }
+};
+
+__device__ __forceinline__ void store_out(void* out, size_t off, const float* v, int n,
+                                          int out_bf16) {
+  if (out_bf16) {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + off;
+    if (n == 8) {
+      uint4 w;
+      __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]);
+      __nv_bfloat162 d = __floats2bfloat162_rn(v[6], v[7]);
+      w.x = *reinterpret_cast<uint32_t*>(&a);
+      w.y = *reinterpret_cast<uint32_t*>(&b);
+      w.z = *reinterpret_cast<uint32_t*>(&c);
+      w.w = *reinterpret_cast<uint32_t*>(&d);
+      *reinterpret_cast<uint4*>(p) = w;
+    } else {
+      for (int e = 0; e < n; ++e) p[e] = __float2bfloat16_rn(v[e]);
+    }
+  } else {
+    float* p = reinterpret_cast<float*>(out) + off;
+    for (int e = 0; e < n; e += 4)
+      *reinterpret_cast<float4*>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+  }
+}
+
+template <typename KV, int D, int G>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using Geo = Geometry<KV, D, G>;
+  using W = WarpAttn<KV, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if ((smem_addr(smem) & 127u) != 0) {  // TMA destinations below assume 128-byte alignment
+    if (threadIdx.x == 0) atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int B = p.B;
+
+  // ---- shared layout: prefix table | stage buffers | barriers | stage info words
+  int32_t* s_pre = reinterpret_cast<int32_t*>(smem);
+  unsigned char* s_stage = smem + p.prefix_bytes;
+  const size_t stage_region = static_cast<size_t>(nwarps) * p.stages * p.stage_bytes;
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_stage + stage_region);
+  int32_t* s_info = reinterpret_cast<int32_t*>(s_bar + nwarps * p.stages);
+
+  // ---- 1. block prefix sums of per-request tile counts (every block computes its own)
+  const int cap_tokens = min(p.max_blocks * kBS, p.max_context_len);
+  {
+    const int per = (B + blockDim.x - 1) / blockDim.x;
+    const int lo = min(B, tid * per), hi = min(B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+      const int L = p.context_lens[b];
+      const bool ok = L >= 0 && L <= cap_tokens;
+      local += ok ? (L + kBS - 1) / kBS : 0;
+    }
+    // block-wide exclusive scan of `local`
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFullMask, incl, d);
+      if (lane >= d) incl += y;
+    }
+    __shared__ int warp_tot[kMaxWarps];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int b = lo; b < hi; ++b) {
+      s_pre[b] = run;
+      const int L = p.context_lens[b];
+      const bool ok = L >= 0 && L <= cap_tokens;
+      run += ok ? (L + kBS - 1) / kBS : 0;
+    }
+    if (tid == blockDim.x - 1) s_pre[B] = run;
+  }
+  // barrier init (one lane per warp, its own stages)
+  if (lane == 0) {
+    for (int s = 0; s < p.stages; ++s) mbar_init(&s_bar[warp * p.stages + s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- 2. rows that get no tiles: empty histories (zeros) and invalid lengths (NaN)
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (s_pre[b + 1] != s_pre[b]) continue;
+    const int L = p.context_lens[b];
+    const bool bad = !(L >= 0 && L <= cap_tokens);
+    if (bad && tid == 0) atomic_or_error(p.error_word, PDA_DEVERR_CONTEXT_LEN);
+    const float val = bad ? __int_as_float(0x7fc00000) : 0.f;
+    for (int i = tid; i < p.H * D; i += blockDim.x) {
+      const size_t off = static_cast<size_t>(b) * p.H * D + i;
+      if (p.out_bf16)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(val);
+      else
+        reinterpret_cast<float*>(p.out)[off] = val;
+    }
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += blockDim.x) p.ws_prefix[i] = s_pre[i];
+
+  // ---- 3. this warp's tile range
+  const int H_kv = p.H_kv;
+  const int W_tiles = s_pre[B] * H_kv;
+  const int NW = p.num_workers;
+  const int w = blockIdx.x * nwarps + warp;
+  const int t_begin = tile_start(w, W_tiles, NW);
+  const int t_end = tile_start(w + 1, W_tiles, NW);
+  if (t_begin >= t_end) return;
+
+  unsigned char* my_stage = s_stage + static_cast<size_t>(warp) * p.stages * p.stage_bytes;
+  uint64_t* my_bar = s_bar + warp * p.stages;
+  int32_t* my_info = s_info + warp * p.stages;
+  auto k_buf = [&](int s) { return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes); };
+  auto v_buf = [&](int s) {
+    return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + Geo::TILE_BYTES);
+  };
+  auto q_buf = [&](int s) {
+    return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
+  };
+
+  // (request, kv-head, block) of tile y
+  auto locate = [&](int y, int& b, int& h, int& blk, int& nb) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] * H_kv <= y) lo = mid; else hi = mid;
+    }
+    b = lo;
+    nb = s_pre[b + 1] - s_pre[b];
+    const int rem = y - s_pre[b] * H_kv;
+    h = rem / nb;
+    blk = rem - h * nb;
+  };
+
+  if (lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  const uint64_t policy = l2_policy_evict_first();
+
+  // Issue-side metadata: lane i describes tile g_base + i.
+  int g_base = -0x40000000;
+  int g_b = 0, g_h = 0, g_blk = 0, g_pid = 0, g_len = 0;
+  auto load_group = [&](int base) {
+    g_base = base;
+    const int y = base + lane;
+    if (y < t_end) {
+      int nb;
+      locate(y, g_b, g_h, g_blk, nb);
+      g_pid = p.block_tables[static_cast<size_t>(g_b) * p.max_blocks + g_blk];
+      g_len = p.context_lens[g_b];
+    }
+  };
+  auto issue = [&](int x, int s) {
+    if (x >= g_base + 32) load_group(x);
+    if (lane == x - g_base) {
+      const bool bad = g_pid < 0 || g_pid >= p.num_blocks;
+      const bool need_q = (g_blk == 0) || (x == t_begin);
+      const int n_valid = min(kBS, g_len - g_blk * kBS);
+      my_info[s] = n_valid | (bad ? 0x100 : 0);
+      if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+      const uint32_t bytes = 2 * Geo::TILE_BYTES + (need_q ? Geo::Q_BYTES : 0);
+      mbar_arrive_expect_tx(&my_bar[s], bytes);
+      const int row = (bad ? 0 : g_pid) * kBS;
+      tma_load_3d(k_buf(s), &tmK, 0, g_h, row, &my_bar[s], policy);
+      tma_load_3d(v_buf(s), &tmV, 0, g_h, row, &my_bar[s], policy);
+      if (need_q) {
+        const KV* src = reinterpret_cast<const KV*>(p.q) +
+                        (static_cast<size_t>(g_b) * p.H + static_cast<size_t>(g_h) * G) * D;
+        bulk_load(q_buf(s), src, Geo::Q_BYTES, &my_bar[s]);
+      }
+    }
+  };
+
+  const int S = p.stages;
+  const int n_tiles = t_end - t_begin;
+  for (int i = 0; i < S && i < n_tiles; ++i) issue(t_begin + i, i);
+
+  // Consumer-side sequential position.
+  int cb, ch, cblk, cnb;
+  locate(t_begin, cb, ch, cblk, cnb);
+  W st;
+  st.init(lane);
+  bool seg_bad = false;
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int x = t_begin; x < t_end; ++x) {
+    const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&my_bar[stage], phase));
+    if (!ready) {
+      atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
+      // Give copies still in flight a bounded chance to land before leaving.
+      for (int y = x; y < min(t_end, x + S); ++y) {
+        const int s2 = (stage + (y - x)) % S;
+        const uint32_t ph2 = phase ^ (((stage + (y - x)) / S) & 1);
+        mbar_wait_bounded(&my_bar[s2], ph2);
+      }
+      return;
+    }
+    const int info = my_info[stage];
+    const int n_valid = info & 0xff;
+    if (cblk == 0 || x == t_begin) {
+      st.reset(q_buf(stage), p.scale_log2);
+      seg_bad = false;
+    }
+    seg_bad |= (info & 0x100) != 0;
+    if (n_valid == kBS)
+      st.template tile<false>(k_buf(stage), v_buf(stage), n_valid);
+    else
+      st.template tile<true>(k_buf(stage), v_buf(stage), n_valid);
+
+    // hand the stage back to the TMA engine
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (x + S < t_end) issue(x + S, stage);
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1;
+    }
+
+    // segment end?
+    const bool last_of_seg = (cblk + 1 == cnb);
+    if (last_of_seg || x + 1 == t_end) {
+      float lj[G], mj[G];
+      st.reduce(lj, mj);
+      const int seg_start = s_pre[cb] * H_kv + ch * cnb;
+      const int seg_end = seg_start + cnb;
+      const bool complete = seg_start >= t_begin && seg_end <= t_end;
+      if (st.rw == 0) {
+        if (complete) {
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            float v[W::VEC];
+            const float inv = seg_bad ? __int_as_float(0x7fc00000) : 1.f / lj[j];
+#pragma unroll
+            for (int e = 0; e < W::VEC; ++e) v[e] = st.o[j][e] * inv;
+            const size_t off =
+                (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D +
+                st.cl * W::VEC;
+            store_out(p.out, off, v, W::VEC, p.out_bf16);
+          }
+        } else {
+          const int slot = 2 * w + (seg_start <= t_begin ? 0 : 1);
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            float* dst = p.ws_o + (static_cast<size_t>(slot) * G + j) * D + st.cl * W::VEC;
+#pragma unroll
+            for (int e = 0; e < W::VEC; e += 4)
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(st.o[j][e], st.o[j][e + 1], st.o[j][e + 2], st.o[j][e + 3]);
+            if (st.cl == 0) {
+              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
+              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
+                  seg_bad ? __int_as_float(0x7fc00000) : lj[j];
+            }
+          }
+        }
+      }
+    }
+    // advance the consumer position
+    if (++cblk == cnb) {
+      cblk = 0;
+      if (++ch == H_kv) {
+        ch = 0;
+        do {
+          ++cb;
+        } while (cb < B && s_pre[cb + 1] == s_pre[cb]);
+      }
+      if (cb < B) cnb = s_pre[cb + 1] - s_pre[cb];
+    }
+  }
+}
+
+struct CombineParams {
+  void* out;
+  const float* ws_o;
+  const float* ws_ml;
+  const int32_t* ws_prefix;
+  int B, H, H_kv, G, D;
+  int num_workers;
+  int out_bf16;
+};
+
+// One warp per (request, kv-head) segment; merges the pieces of segments that were cut by
+// worker-range boundaries:  M = max m_j,  L = sum l_j 2^(m_j - M),
+// out = sum o_j 2^(m_j - M) / L.
+__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const int seg = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (seg >= p.B * p.H_kv) return;
+  const int b = seg / p.H_kv, h = seg % p.H_kv;
+  const int nb = p.ws_prefix[b + 1] - p.ws_prefix[b];
+  if (nb == 0) return;
+  const int W = p.ws_prefix[p.B] * p.H_kv;
+  const int NW = p.num_workers;
+  const int S = p.ws_prefix[b] * p.H_kv + h * nb;
+  const int E = S + nb;
+  const int w0 = tile_owner(S, W, NW), w1 = tile_owner(E - 1, W, NW);
+  if (w0 == w1) return;
+  const bool w0_tail = S != tile_start(w0, W, NW);
+  const int G = p.G, D = p.D;
+  for (int j = 0; j < G; ++j) {
+    float M = -INFINITY;
+    for (int w = w0; w <= w1; ++w) {
+      if (tile_start(w, W, NW) == tile_start(w + 1, W, NW)) continue;
+      const int slot = 2 * w + ((w == w0 && w0_tail) ? 1 : 0);
+      M = fmaxf(M, p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2]);
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float Lsum = 0.f;
+    const int per = D / 32;
+    for (int w = w0; w <= w1; ++w) {
+      if (tile_start(w, W, NW) == tile_start(w + 1, W, NW)) continue;
+      const int slot = 2 * w + ((w == w0 && w0_tail) ? 1 : 0);
+      const float m = p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2];
+      const float l = p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1];
+      const float f = ex2(m - M);
+      Lsum += l * f;
+      const float* o = p.ws_o + (static_cast<size_t>(slot) * G + j) * D;
+      for (int e = 0; e < per; ++e) acc[e] += o[lane + 32 * e] * f;
+    }
+    const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
+    for (int e = 0; e < per; ++e) {
+      const float v = acc[e] / Lsum;
+      if (p.out_bf16)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
+      else
+        reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+struct LaunchPlan {
+  int nwarps, stages, grid;
+  uint32_t stage_bytes, prefix_bytes;
+  size_t smem_bytes;
+  size_t ws_prefix, ws_ml, ws_o, ws_total;  // byte offsets / total
+};
+
+uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
+  const uint32_t e = static_cast<uint32_t>(dtype_bytes(kv));
+  const uint32_t tile = kBS * D * e;
+  return 2 * tile + static_cast<uint32_t>(round_up(static_cast<size_t>(G) * D * e, 128));
+}
+
+bool make_plan(int B, int G, int D, pda_dtype kv, int sm_cap, int num_sms, LaunchPlan* pl) {
+  pl->stage_bytes = stage_bytes_for(kv, D, G);
+  pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, 128));
+  pl->nwarps = 0;
+  for (int nw = kMaxWarps; nw >= 2; nw /= 2) {
+    const size_t fixed = pl->prefix_bytes;
+    const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
+    if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
+    const int stages = static_cast<int>((kSmemBudget - fixed) / per_stage);
+    if (stages >= 2) {
+      pl->nwarps = nw;
+      pl->stages = stages > 4 ? 4 : stages;
+      break;
+    }
+  }
+  if (pl->nwarps == 0) return false;
+  size_t smem = pl->prefix_bytes +
+                static_cast<size_t>(pl->nwarps) * pl->stages * (pl->stage_bytes + 8 + 4);
+  smem = round_up(smem, 128);
+  if (smem < static_cast<size_t>(kMinResidentSmem)) smem = kMinResidentSmem;
+  pl->smem_bytes = smem;
+  int grid = num_sms;
+  if (sm_cap > 0 && sm_cap < grid) grid = sm_cap;
+  pl->grid = grid;
+  const size_t nw_total = static_cast<size_t>(grid) * pl->nwarps;
+  pl->ws_prefix = 0;
+  pl->ws_ml = round_up(static_cast<size_t>(B + 1) * 4, 256);
+  pl->ws_o = pl->ws_ml + round_up(2 * nw_total * G * 2 * 4, 256);
+  pl->ws_total = pl->ws_o + round_up(2 * nw_total * G * static_cast<size_t>(D) * 4, 256);
+  return true;
+}
+
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnParams);
+
+template <typename KV, int D>
+KernelFn pick_g(int G) {
+  switch (G) {
+    case 1: return attn_partial_kernel<KV, D, 1>;
+    case 2: return attn_partial_kernel<KV, D, 2>;
+    case 4: return attn_partial_kernel<KV, D, 4>;
+    case 8: return attn_partial_kernel<KV, D, 8>;
+    default: return nullptr;
+  }
+}
+
+KernelFn pick_kernel(pda_dtype kv, int D, int G) {
+  if (kv == PDA_BF16) {
+    if (D == 128) return pick_g<__nv_bfloat16, 128>(G);
+    if (D == 64) return pick_g<__nv_bfloat16, 64>(G);
+  } else {
+    if (D == 128) return pick_g<float, 128>(G);
+    if (D == 64) return pick_g<float, 64>(G);
+  }
+  return nullptr;
+}
+
+bool supported_g(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+
+}  // namespace
+}  // namespace pda
+
+using namespace pda;
+
+extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block_size,
+                                                   pda_dtype kv_dtype, int sm_cap,
+                                                   size_t* bytes) {
+  if (bytes == nullptr || B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 ||
+      block_size <= 0 || sm_cap < 0 || !dtype_ok(kv_dtype))
+    return PDA_ERR_INVALID_ARG;
+  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(H / H_kv) || B > kMaxBatch)
+    return PDA_ERR_UNSUPPORTED;
+  int dev, sms;
+  const pda_status st = current_device_sms(&dev, &sms);
+  if (st != PDA_OK) return st;
+  LaunchPlan pl;
+  if (!make_plan(B, H / H_kv, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  *bytes = pl.ws_total;
+  return PDA_OK;
+}
+
+extern "C" pda_status pda_paged_decode_attention(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
+    float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
+    void* workspace, size_t workspace_bytes, int32_t* error_word, cudaStream_t stream) {
+  // ---- host-side validation, before any CUDA call
+  if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || sm_cap < 0 ||
+      !dtype_ok(q_dtype) || !dtype_ok(kv_dtype) || !dtype_ok(out_dtype) || !isfinite(scale))
+    return PDA_ERR_INVALID_ARG;
+  if (B == 0) return PDA_OK;
+  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      block_tables == nullptr || context_lens == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PDA_ERR_INVALID_ARG;
+  const int G = H / H_kv;
+  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(G) || q_dtype != kv_dtype ||
+      B > kMaxBatch)
+    return PDA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31) ||
+      static_cast<long long>(B) * max_blocks_per_seq * H_kv >= (1ll << 31))
+    return PDA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PDA_ERR_WORKSPACE;
+
+  int dev, sms;
+  pda_status st = current_device_sms(&dev, &sms);
+  if (st != PDA_OK) return st;
+  LaunchPlan pl;
+  if (!make_plan(B, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
+
+  KernelFn fn = pick_kernel(kv_dtype, D, G);
+  if (fn == nullptr) return PDA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
+    return PDA_ERR_CUDA;
+
+  CUtensorMap tmK, tmV;
+  st = encode_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  if (st != PDA_OK) return st;
+  st = encode_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  if (st != PDA_OK) return st;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  AttnParams ap;
+  ap.out = out;
+  ap.q = q;
+  ap.block_tables = block_tables;
+  ap.context_lens = context_lens;
+  ap.ws_prefix = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
+  ap.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
+  ap.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
+  ap.error_word = error_word;
+  ap.B = B;
+  ap.H = H;
+  ap.H_kv = H_kv;
+  ap.num_blocks = num_blocks;
+  ap.max_blocks = max_blocks_per_seq;
+  ap.max_context_len = max_context_len;
+  ap.out_bf16 = out_dtype == PDA_BF16;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.num_workers = pl.grid * pl.nwarps;
+  ap.stages = pl.stages;
+  ap.stage_bytes = pl.stage_bytes;
+  ap.prefix_bytes = pl.prefix_bytes;
+
+  fn<<<pl.grid, pl.nwarps * 32, pl.smem_bytes, stream>>>(tmK, tmV, ap);
+  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+
+  CombineParams cp;
+  cp.out = out;
+  cp.ws_o = ap.ws_o;
+  cp.ws_ml = ap.ws_ml;
+  cp.ws_prefix = ap.ws_prefix;
+  cp.B = B;
+  cp.H = H;
+  cp.H_kv = H_kv;
+  cp.G = G;
+  cp.D = D;
+  cp.num_workers = ap.num_workers;
+  cp.out_bf16 = ap.out_bf16;
+  const int segs = B * H_kv;
+  attn_combine_kernel<<<(segs + 3) / 4, 128, 0, stream>>>(cp);
+  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  return PDA_OK;
+}

@@ -1,0 +1,211 @@
+// kv_ops.cu -- KV append (scatter of each request's new token into its slot) and KV pack
+// (gather of one request's scattered blocks into a contiguous transfer buffer), sm_103a.
+//
+// Both are pure copies of rows of H_kv * D elements, done as 16-byte vectors with
+// streaming (evict-first) loads and stores so a large pack does not flush L2.
+//  * append: each decode step writes the new token's K/V (page "Disaggregated LLM
+//    Serving: from PD disaggregation to attention offload", sec. 1, second list item 2)
+//    into slot s = block * block_size + row, i.e. block s / block_size, row s % block_size.
+//  * pack: request-level KV transfer needs the request's KV in one buffer (page on goodput
+//    and PD disaggregation, 0539edu.com, sec. 5.4); out[t] = (K row, V row) of token t,
+//    token t being row t % block_size of block table[t / block_size].
+#include "pda_device.cuh"
+#include "pda_internal.h"
+
+namespace pda {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict__ k_new,
+                                                        const uint4* __restrict__ v_new,
+                                                        uint4* __restrict__ k_cache,
+                                                        uint4* __restrict__ v_cache,
+                                                        const int32_t* __restrict__ slots, int B,
+                                                        int row_vecs, int block_size,
+                                                        int num_blocks, int32_t* error_word) {
+  const long long total = static_cast<long long>(B) * 2 * row_vecs;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(i / (2 * row_vecs));
+    const int rem = static_cast<int>(i % (2 * row_vecs));
+    const int which = rem / row_vecs;  // 0: K, 1: V
+    const int c = rem % row_vecs;
+    const int s = slots[b];
+    if (s < 0) continue;  // padding
+    const long long block = s / block_size;
+    const long long row = s % block_size;
+    if (block >= num_blocks) {
+      if (rem == 0) atomic_or_error(error_word, PDA_DEVERR_SLOT);
+      continue;
+    }
+    const size_t dst = static_cast<size_t>(block * block_size + row) * row_vecs + c;
+    const size_t src = static_cast<size_t>(b) * row_vecs + c;
+    if (which == 0)
+      k_cache[dst] = k_new[src];
+    else
+      v_cache[dst] = v_new[src];
+  }
+}
+
+struct PackJob {
+  uint4* out;
+  const int32_t* table;
+  int len;
+};
+
+struct PackParams {
+  const uint4* k_cache;
+  const uint4* v_cache;
+  int32_t* error_word;
+  int n, row_vecs, block_size, num_blocks;
+  PackJob jobs[PDA_PACK_MAX_BATCH];
+};
+
+constexpr int kPackUnroll = 4;
+
+// blockIdx.y selects the request; the x-dimension strides over its (token, K|V, vector)
+// copies with kPackUnroll independent 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256) kv_pack_kernel(const __grid_constant__ PackParams p) {
+  const PackJob job = p.jobs[blockIdx.y];
+  const int rv = p.row_vecs;
+  const long long total = static_cast<long long>(job.len) * 2 * rv;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x * kPackUnroll;
+  for (long long base = blockIdx.x * static_cast<long long>(blockDim.x) * kPackUnroll +
+                        threadIdx.x;
+       base < total; base += step) {
+    uint4 v[kPackUnroll];
+    bool bad[kPackUnroll];
+#pragma unroll
+    for (int u = 0; u < kPackUnroll; ++u) {
+      const long long i = base + static_cast<long long>(u) * blockDim.x;
+      bad[u] = false;
+      if (i < total) {
+        const int t = static_cast<int>(i / (2 * rv));
+        const int rem = static_cast<int>(i % (2 * rv));
+        const int which = rem / rv;
+        const int c = rem % rv;
+        const int blk = job.table[t / p.block_size];
+        if (blk < 0 || blk >= p.num_blocks) {
+          bad[u] = true;
+          v[u] = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+        } else {
+          const size_t src =
+              (static_cast<size_t>(blk) * p.block_size + t % p.block_size) * rv + c;
+          v[u] = __ldcs(which == 0 ? p.k_cache + src : p.v_cache + src);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPackUnroll; ++u) {
+      const long long i = base + static_cast<long long>(u) * blockDim.x;
+      if (i < total) {
+        if (bad[u] && (i % (2 * rv)) == 0) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+        __stcs(job.out + i, v[u]);
+      }
+    }
+  }
+}
+
+namespace {
+
+pda_status check_kv_rows(int H_kv, int D, int block_size, int num_blocks, pda_dtype dt,
+                         int* row_vecs) {
+  if (H_kv <= 0 || D <= 0 || block_size <= 0 || num_blocks <= 0 || !dtype_ok(dt))
+    return PDA_ERR_INVALID_ARG;
+  const size_t row_bytes = static_cast<size_t>(H_kv) * D * dtype_bytes(dt);
+  if (row_bytes % 16 != 0 || row_bytes / 16 > (1u << 28)) return PDA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return PDA_ERR_UNSUPPORTED;
+  *row_vecs = static_cast<int>(row_bytes / 16);
+  return PDA_OK;
+}
+
+pda_status launch_pack(const PackParams& p, long long max_total, cudaStream_t stream) {
+  const long long per_block = 256ll * kPackUnroll;
+  long long gx = (max_total + per_block - 1) / per_block;
+  if (gx > 4096) gx = 4096;
+  if (gx < 1) gx = 1;
+  kv_pack_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.n)), 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pda
+
+using namespace pda;
+
+extern "C" pda_status pda_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                                    void* v_cache, const int32_t* slot_mapping, int B, int H_kv,
+                                    int D, int block_size, int num_blocks, pda_dtype kv_dtype,
+                                    int32_t* error_word, cudaStream_t stream) {
+  if (B < 0) return PDA_ERR_INVALID_ARG;
+  int rv = 0;
+  const pda_status st = check_kv_rows(H_kv, D, block_size, num_blocks, kv_dtype, &rv);
+  if (st != PDA_OK) return st;
+  if (B == 0) return PDA_OK;
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      slot_mapping == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PDA_ERR_INVALID_ARG;
+  const long long total = static_cast<long long>(B) * 2 * rv;
+  long long grid = (total + 255) / 256;
+  if (grid > 65535) grid = 65535;
+  kv_append_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, B, rv,
+      block_size, num_blocks, error_word);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
+extern "C" pda_status pda_kv_pack_blocks_batched(void* const* outs,
+                                                 const int32_t* const* block_table_rows,
+                                                 const int32_t* context_lens, int n,
+                                                 const void* k_cache, const void* v_cache,
+                                                 int H_kv, int D, int block_size, int num_blocks,
+                                                 pda_dtype kv_dtype, int32_t* error_word,
+                                                 cudaStream_t stream) {
+  if (n < 0 || n > PDA_PACK_MAX_BATCH) return n < 0 ? PDA_ERR_INVALID_ARG : PDA_ERR_UNSUPPORTED;
+  int rv = 0;
+  const pda_status st = check_kv_rows(H_kv, D, block_size, num_blocks, kv_dtype, &rv);
+  if (st != PDA_OK) return st;
+  if (n == 0) return PDA_OK;
+  if (outs == nullptr || block_table_rows == nullptr || context_lens == nullptr ||
+      k_cache == nullptr || v_cache == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PDA_ERR_INVALID_ARG;
+  PackParams p;
+  p.k_cache = static_cast<const uint4*>(k_cache);
+  p.v_cache = static_cast<const uint4*>(v_cache);
+  p.error_word = error_word;
+  p.row_vecs = rv;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  int m = 0;
+  long long max_total = 0;
+  for (int i = 0; i < n; ++i) {
+    const int len = context_lens[i];
+    if (len < 0) return PDA_ERR_INVALID_ARG;
+    if (len == 0) continue;
+    if (outs[i] == nullptr || block_table_rows[i] == nullptr || !aligned16(outs[i]))
+      return PDA_ERR_INVALID_ARG;
+    p.jobs[m].out = static_cast<uint4*>(outs[i]);
+    p.jobs[m].table = block_table_rows[i];
+    p.jobs[m].len = len;
+    const long long tot = static_cast<long long>(len) * 2 * rv;
+    if (tot > max_total) max_total = tot;
+    ++m;
+  }
+  if (m == 0) return PDA_OK;
+  p.n = m;
+  return launch_pack(p, max_total, stream);
+}
+
+extern "C" pda_status pda_kv_pack_blocks(void* out, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table_row, int context_len,
+                                         int H_kv, int D, int block_size, int num_blocks,
+                                         pda_dtype kv_dtype, int32_t* error_word,
+                                         cudaStream_t stream) {
+  void* outs[1] = {out};
+  const int32_t* rows[1] = {block_table_row};
+  const int32_t lens[1] = {context_len};
+  return pda_kv_pack_blocks_batched(outs, rows, lens, 1, k_cache, v_cache, H_kv, D, block_size,
+                                    num_blocks, kv_dtype, error_word, stream);
+}

@@ -1,0 +1,88 @@
+// pda_api.cu -- host-side helpers of the C ABI: status names, device SM counts and the
+// TMA tensor-map encoder (obtained from the driver through the runtime, no -lcuda).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pda_internal.h"
+
+namespace pda {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encoder() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+}  // namespace
+
+pda_status current_device_sms(int* device, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  *device = dev;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int cached = g_sms[dev].load(std::memory_order_relaxed);
+    if (cached > 0) {
+      *num_sms = cached;
+      return PDA_OK;
+    }
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return PDA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) g_sms[dev].store(sms, std::memory_order_relaxed);
+  *num_sms = sms;
+  return PDA_OK;
+}
+
+pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
+                                int block_size, int H_kv, int D, pda_dtype dtype) {
+  std::call_once(g_encode_once, load_encoder);
+  if (g_encode == nullptr) return PDA_ERR_CUDA;
+  const cuuint64_t e = dtype_bytes(dtype);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
+                              static_cast<cuuint64_t>(num_blocks) * block_size};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e,
+                                 static_cast<cuuint64_t>(H_kv) * D * e};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(block_size)};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType dt =
+      dtype == PDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUresult r = g_encode(tm, dt, 3, const_cast<void*>(base), dims, strides, box,
+                              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
+}
+
+}  // namespace pda
+
+extern "C" const char* pda_status_string(pda_status status) {
+  switch (status) {
+    case PDA_OK: return "ok";
+    case PDA_ERR_INVALID_ARG: return "invalid argument";
+    case PDA_ERR_UNSUPPORTED: return "unsupported shape, dtype or size";
+    case PDA_ERR_CUDA: return "CUDA runtime error";
+    case PDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+extern "C" int pda_version(void) { return 1; }
+
+extern "C" pda_status pda_device_sm_count(int* num_sms) {
+  if (num_sms == nullptr) return PDA_ERR_INVALID_ARG;
+  int dev;
+  return pda::current_device_sms(&dev, num_sms);
+}

@@ -1,0 +1,26 @@
+// pda_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pda.h"
+
+namespace pda {
+
+// SM count of the current device (cached per device). Returns PDA_ERR_CUDA on failure.
+pda_status current_device_sms(int* device, int* num_sms);
+
+// Encodes a 3-D tiled tensor map over a KV cache [num_blocks * block_size, H_kv, D]
+// (innermost first: D, H_kv, rows) with box {D, 1, block_size}.
+pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
+                                int block_size, int H_kv, int D, pda_dtype dtype);
+
+inline size_t dtype_bytes(pda_dtype t) { return t == PDA_BF16 ? 2u : 4u; }
+inline bool dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace pda

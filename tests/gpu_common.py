@@ -1,0 +1,90 @@
+"""Shared helpers of the GPU parity tests: host copies for the oracle, the GPU step through
+the C ABI, and the attention tolerance check."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import paged_decode_attention_02_gb300 as pda
+from oracle import oracle as orc
+
+# Attention tolerance for bf16 output: max abs error 4e-3, and max of
+# |got - ref| / max(|ref|, 1e-2) at most 1e-2 (the floor keeps near-zero outputs from
+# turning fp32 accumulation noise into huge ratios).
+ABS_TOL, REL_TOL, REL_FLOOR = 4e-3, 1e-2, 1e-2
+# fp32 output: fp32 accumulation and a 2^-22 exp2 approximation; far inside 1e-4.
+F32_ABS_TOL = 1e-4
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = ""):
+    g = got.detach().double().cpu().numpy()
+    nan_ref = np.isnan(ref)
+    assert np.array_equal(np.isnan(g), nan_ref), f"{what}: NaN pattern differs"
+    ok = ~nan_ref
+    if not ok.any():
+        return
+    err = np.abs(g[ok] - ref[ok])
+    rel = err / np.maximum(np.abs(ref[ok]), REL_FLOOR)
+    abs_tol = F32_ABS_TOL if got.dtype == torch.float32 else ABS_TOL
+    assert err.max() <= abs_tol, f"{what}: max abs err {err.max():.3e} > {abs_tol}"
+    assert rel.max() <= REL_TOL, f"{what}: max rel err {rel.max():.3e} > {REL_TOL}"
+
+
+def oracle_full_step(s, append: bool = True, num_threads: int = 0):
+    """fp64 oracle of the whole step on host copies taken before the GPU runs."""
+    kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
+    if append:
+        assert orc.kv_append(to_np(s.k_new), to_np(s.v_new), kc, vc, s.slot_mapping_np) == 0
+    ref, st = orc.paged_decode_attention(to_np(s.q), kc, vc, s.block_tables_np,
+                                         s.context_lens_np, s.scale, num_threads=num_threads)
+    return ref, st, kc, vc
+
+
+def oracle_sampled(s, reqs, append: bool = True):
+    """Oracle of requests ``reqs`` only: their blocks are fetched into a small host pool
+    (renumbered), so full-size workloads need not be copied whole. Call before the GPU
+    step mutates the caches."""
+    bs = s.w.block_size
+    reqs = list(reqs)
+    nblk = [(int(s.context_lens_np[r]) + bs - 1) // bs for r in reqs]
+    used = sorted({int(s.block_tables_np[r, j]) for r, n in zip(reqs, nblk) for j in range(n)})
+    pos = {b: i for i, b in enumerate(used)}
+    idx = torch.tensor(used if used else [0], dtype=torch.long, device=s.k_cache.device)
+    kc = to_np(s.k_cache.index_select(0, idx)).copy()
+    vc = to_np(s.v_cache.index_select(0, idx)).copy()
+    mb = max(1, max(nblk) if nblk else 1)
+    bt = np.full((len(reqs), mb), -1, np.int32)
+    for i, (r, n) in enumerate(zip(reqs, nblk)):
+        bt[i, :n] = [pos[int(b)] for b in s.block_tables_np[r, :n]]
+    lens = s.context_lens_np[reqs].astype(np.int32)
+    if append:
+        slots = np.full(len(reqs), -1, np.int32)
+        for i, r in enumerate(reqs):
+            sl = int(s.slot_mapping_np[r])
+            if sl >= 0:
+                slots[i] = pos[sl // bs] * bs + sl % bs
+        st = orc.kv_append(to_np(s.k_new[reqs]), to_np(s.v_new[reqs]), kc, vc, slots)
+        assert st == 0
+    q = to_np(s.q[reqs]).copy()
+    ref, st = orc.paged_decode_attention(q, kc, vc, bt, lens, s.scale)
+    return ref, st
+
+
+def gpu_step(s, append: bool = True, sm_cap: int = 0, out_dtype=None, workspace=None):
+    """kv_append then paged_decode_attention through the C ABI; returns (out, error word)."""
+    err = torch.zeros(1, dtype=torch.int32, device=s.q.device)
+    if append:
+        pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+    out = torch.empty(s.q.shape, dtype=out_dtype or s.q.dtype, device=s.q.device)
+    pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens,
+                               s.max_context_len, s.scale, sm_cap=sm_cap, workspace=workspace,
+                               error_word=err)
+    torch.cuda.synchronize()
+    return out, int(err.item())

@@ -1,0 +1,305 @@
+"""CUDA path against the fp64 oracle, through the C ABI, on seeded inputs.
+
+append and pack are compared bit for bit; attention within max-abs 4e-3 and floored
+max-rel 1e-2 (bf16 output) or 1e-4 abs (fp32 output). Small cases compare every output;
+the full-size workloads, in the launch configuration the benchmark times, compare sampled
+requests (longest, shortest and random ones) that the oracle computes one by one.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import paged_decode_attention_02_gb300 as pda
+from gpu_common import (assert_attention_close, gpu_step, oracle_full_step, oracle_sampled,
+                        to_np)
+from oracle import oracle as orc
+from paged_decode_attention_02_gb300 import binding
+from paged_decode_attention_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+def variant(base: str, **kw) -> wl.Workload:
+    return dataclasses.replace(wl.get(base), **kw)
+
+
+# ------------------------------------------------------------------ whole workloads
+def test_tiny_full_step():
+    s = wl.make_step("tiny", device=DEV)
+    ref, st, kc, vc = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
+    assert_attention_close(out, ref, "tiny")
+    # ctx = 1 returns the appended V exactly (fp32 all the way)
+    b1 = int(np.where(s.context_lens_np == 1)[0][0])
+    for h in range(s.w.H):
+        assert torch.equal(out[b1, h], s.v_new[b1, h // s.w.group])
+
+
+def test_llama2_7b_b8_every_output():
+    s = wl.make_step("llama2_7b_b8", device=DEV)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, "llama2_7b_b8")
+
+
+@pytest.mark.parametrize("name,B", [("llama2_13b_b80", 12), ("gqa_skew_b256", 24),
+                                    ("sm_sweep_b128", 16)])
+def test_reduced_batch_every_output(name, B):
+    s = wl.make_step(name, device=DEV, B=B)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, name)
+
+
+def _sample(s, k=10, seed=0):
+    L = s.context_lens_np
+    rng = np.random.default_rng(seed)
+    picks = {int(np.argmax(L)), int(np.argmin(L))}
+    picks |= {int(x) for x in rng.choice(len(L), size=min(k, len(L)), replace=False)}
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["llama2_13b_b80", "gqa_skew_b256", "sm_sweep_b128"])
+def test_full_size_sampled(name):
+    s = wl.make_step(name, device=DEV)
+    reqs = _sample(s)
+    ref, st = oracle_sampled(s, reqs)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out[reqs], ref, name)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_full_size_pack_of_longest_requests():
+    s = wl.make_step("gqa_skew_b256", device=DEV)
+    reqs = s.pack_requests
+    assert len(reqs) == 8
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+    outs = [torch.empty((int(s.context_lens_np[r]), 2, s.w.H_kv, s.w.D), dtype=s.k_cache.dtype,
+                        device=DEV) for r in reqs]
+    pda.kv_pack_blocks_batched(outs, s.k_cache, s.v_cache, [s.block_tables[r] for r in reqs],
+                               [int(s.context_lens_np[r]) for r in reqs], error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # expected: the oracle's pack over host copies of each request's blocks
+    bs = s.w.block_size
+    for r, o in zip(reqs, outs):
+        L = int(s.context_lens_np[r])
+        n = (L + bs - 1) // bs
+        blocks = torch.from_numpy(s.block_tables_np[r, :n].astype(np.int64)).to(DEV)
+        kc = to_np(s.k_cache.index_select(0, blocks)).copy()
+        vc = to_np(s.v_cache.index_select(0, blocks)).copy()
+        want, st = orc.kv_pack_blocks(kc, vc, np.arange(n, dtype=np.int32), L)
+        assert st == 0
+        assert np.array_equal(to_np(o).view(np.uint8), want.view(np.uint8)), r
+
+
+# ------------------------------------------------------------------ shapes and dtypes
+SHAPES = [  # (dtype, D, H, H_kv)
+    ("bf16", 128, 32, 32), ("bf16", 128, 32, 16), ("bf16", 128, 32, 8), ("bf16", 128, 32, 4),
+    ("bf16", 64, 16, 16), ("bf16", 64, 16, 8), ("bf16", 64, 16, 4), ("bf16", 64, 16, 2),
+    ("f32", 64, 8, 8), ("f32", 64, 8, 2), ("f32", 128, 8, 8), ("f32", 128, 16, 2),
+]
+
+
+@pytest.mark.parametrize("dtype,D,H,H_kv", SHAPES)
+def test_shapes_and_groups(dtype, D, H, H_kv):
+    w = variant("llama2_13b_b80", dtype=dtype, D=D, H=H, H_kv=H_kv, B=9,
+                lengths="uniform:1,700")
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, 700, 255], np.int32)
+    s = wl.make_step(w, device=DEV, lengths=lens)
+    ref, st, kc, vc = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert np.array_equal(to_np(s.k_cache), kc)
+    assert_attention_close(out, ref, f"{dtype} D={D} H={H} H_kv={H_kv}")
+
+
+def test_bf16_inputs_fp32_output():
+    s = wl.make_step("llama2_13b_b80", device=DEV, B=6)
+    ref, _, _, _ = oracle_full_step(s)
+    out, err = gpu_step(s, out_dtype=torch.float32)
+    assert err == 0
+    assert_attention_close(out, ref, "bf16 in, f32 out")
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_and_single_token_histories():
+    lens = np.array([0, 1, 0, 2, 1, 16, 0], np.int32)
+    s = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=7)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, "empty/single")
+    assert (out[lens == 0] == 0).all()
+    for b in np.where(lens == 1)[0]:
+        assert torch.equal(out[b], s.v_new[b].to(out.dtype))  # exact: p = 1
+
+
+def test_all_empty_batch():
+    s = wl.make_step("llama2_13b_b80", device=DEV, lengths=np.zeros(5, np.int32), B=5)
+    out, err = gpu_step(s, append=False)
+    assert err == 0 and (out == 0).all()
+
+
+def test_single_very_long_request_split_over_every_worker():
+    w = variant("gqa_skew_b256", B=1)
+    s = wl.make_step(w, device=DEV, lengths=np.array([32768], np.int32))
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, "B=1 L=32768")
+
+
+def test_many_one_block_requests():
+    lens = np.random.default_rng(3).integers(1, 17, size=600).astype(np.int32)
+    w = variant("gqa_skew_b256", B=600)
+    s = wl.make_step(w, device=DEV, lengths=lens)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, "600 one-block requests")
+
+
+def test_unused_rows_poisoned_with_nan_are_never_read():
+    lens = np.array([5, 16, 17, 40, 1, 100], np.int32)
+    s = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=6, poison_unused=True)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0 and np.isfinite(ref).all()
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert_attention_close(out, ref, "poisoned")
+
+
+def test_shared_prefix_blocks_give_identical_rows():
+    s = wl.make_step("llama2_13b_b80", device=DEV, B=4)
+    s.block_tables[1] = s.block_tables[0]
+    s.block_tables_np[1] = s.block_tables_np[0]
+    s.context_lens[1] = s.context_lens[0]
+    s.context_lens_np[1] = s.context_lens_np[0]
+    s.q[1] = s.q[0]
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert torch.equal(out[0], out[1])
+    ref, _, _, _ = oracle_full_step(s, append=False)
+    assert_attention_close(out, ref, "shared prefix")
+
+
+@pytest.mark.parametrize("cap", [1, 2, 15, 30, 61, 91, 152, 1000])
+def test_sm_cap_does_not_change_results(cap):
+    s = wl.make_step("sm_sweep_b128", device=DEV, B=10)
+    ref, _, _, _ = oracle_full_step(s)
+    out, err = gpu_step(s, sm_cap=cap)
+    assert err == 0
+    assert_attention_close(out, ref, f"sm_cap={cap}")
+
+
+def test_repeat_runs_are_bitwise_identical():
+    s = wl.make_step("gqa_skew_b256", device=DEV, B=32)
+    a, _ = gpu_step(s, append=False)
+    b, _ = gpu_step(s, append=False)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ device-side errors
+def test_bad_block_id_gives_nan_rows_and_error_bit():
+    lens = np.array([40, 40, 40], np.int32)
+    w = variant("gqa_skew_b256", B=3)
+    s = wl.make_step(w, device=DEV, lengths=lens)
+    s.block_tables[1, 1] = s.num_blocks + 7
+    out, err = gpu_step(s, append=False)
+    assert err & binding.PDA_DEVERR_BLOCK_ID
+    assert torch.isnan(out[1].float()).all()
+    assert torch.isfinite(out[0].float()).all() and torch.isfinite(out[2].float()).all()
+
+
+def test_context_beyond_capacity_gives_nan_rows_and_error_bit():
+    lens = np.array([20, 30], np.int32)
+    s = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=2)
+    s.context_lens[0] = s.max_blocks * 16 + 1
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty_like(s.q)
+    pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens,
+                               10 ** 6, s.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & binding.PDA_DEVERR_CONTEXT_LEN
+    assert torch.isnan(out[0].float()).all() and torch.isfinite(out[1].float()).all()
+
+
+def test_context_beyond_declared_max_is_an_error():
+    s = wl.make_step("llama2_13b_b80", device=DEV, lengths=np.array([64, 64], np.int32), B=2)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty_like(s.q)
+    pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens,
+                               32, s.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & binding.PDA_DEVERR_CONTEXT_LEN
+    assert torch.isnan(out.float()).all()
+
+
+def test_append_slot_out_of_range_and_padding():
+    s = wl.make_step("tiny", device=DEV)
+    before_k = s.k_cache.clone()
+    s.slot_mapping[0] = -1                       # padding: skipped silently
+    s.slot_mapping[1] = s.num_blocks * 16 + 3    # out of range: error bit, skipped
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == binding.PDA_DEVERR_SLOT
+    kc = to_np(before_k).copy()
+    vc = to_np(s.v_cache).copy()  # only compared for K below
+    sm = s.slot_mapping.cpu().numpy()
+    sm_ok = np.where((sm >= 0) & (sm < s.num_blocks * 16), sm, -1).astype(np.int32)
+    orc.kv_append(to_np(s.k_new), to_np(s.v_new), kc, vc, sm_ok)
+    assert np.array_equal(to_np(s.k_cache), kc)
+
+
+def test_pack_bad_block_sets_error_and_nan_pattern():
+    s = wl.make_step("tiny", device=DEV)
+    b = 3
+    L = int(s.context_lens_np[b])
+    s.block_tables[b, 2] = -5
+    out = torch.zeros((L, 2, s.w.H_kv, s.w.D), dtype=s.k_cache.dtype, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_pack_blocks(out, s.k_cache, s.v_cache, s.block_tables[b], L, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == binding.PDA_DEVERR_BLOCK_ID
+    bad = to_np(out[32:48]).view(np.uint8)
+    assert (bad == 0xFF).all()
+    kc, vc = to_np(s.k_cache), to_np(s.v_cache)
+    want, _ = orc.kv_pack_blocks(kc, vc, s.block_tables_np[b], 32)
+    assert np.array_equal(to_np(out[:32]).view(np.uint8), want.view(np.uint8))
+
+
+def test_workspace_too_small_is_rejected():
+    s = wl.make_step("tiny", device=DEV)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(s.q)
+    with pytest.raises(binding.PdaError) as e:
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                   s.context_lens, s.max_context_len, s.scale, workspace=ws)
+    assert e.value.status == binding.PDA_ERR_WORKSPACE
