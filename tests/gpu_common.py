@@ -11,6 +11,10 @@ from oracle import oracle as orc
 # Attention tolerance for bf16 output: max abs error 4e-3, and max of
 # |got - ref| / max(|ref|, 1e-2) at most 1e-2 (the floor keeps near-zero outputs from
 # turning fp32 accumulation noise into huge ratios).
+# Where |ref| > 2.05, rounding even the exact result to bf16 can move it by more than
+# 4e-3 (half a bf16 ulp is 2^-8 * 2^floor(log2 |ref|)). There the absolute bound is half a
+# bf16 ulp of the reference plus 1e-5 |ref| for the fp32 accumulation that precedes the
+# rounding; the relative bound is unchanged everywhere.
 ABS_TOL, REL_TOL, REL_FLOOR = 4e-3, 1e-2, 1e-2
 # fp32 output: fp32 accumulation and a 2^-22 exp2 approximation; far inside 1e-4.
 F32_ABS_TOL = 1e-4
@@ -23,7 +27,15 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = ""):
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers (8 significant bits) at |x|."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 8)
+
+
+def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = "",
+                           strict: bool = False):
+    """``strict``: the flat 4e-3 bound everywhere (the named workloads, where |ref| < 2.05)."""
     g = got.detach().double().cpu().numpy()
     nan_ref = np.isnan(ref)
     assert np.array_equal(np.isnan(g), nan_ref), f"{what}: NaN pattern differs"
@@ -32,8 +44,16 @@ def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = ""):
         return
     err = np.abs(g[ok] - ref[ok])
     rel = err / np.maximum(np.abs(ref[ok]), REL_FLOOR)
-    abs_tol = F32_ABS_TOL if got.dtype == torch.float32 else ABS_TOL
-    assert err.max() <= abs_tol, f"{what}: max abs err {err.max():.3e} > {abs_tol}"
+    r = ref[ok]
+    if got.dtype == torch.float32:
+        bound = np.full_like(r, F32_ABS_TOL)
+    elif strict:
+        bound = np.full_like(r, ABS_TOL)
+    else:
+        bound = np.maximum(ABS_TOL, bf16_half_ulp(r) + 1e-5 * np.abs(r))
+    worst = int(np.argmax(err - bound))
+    assert err[worst] <= bound[worst], (
+        f"{what}: abs err {err[worst]:.3e} > bound {bound[worst]:.3e} at |ref| {abs(r[worst]):.3f}")
     assert rel.max() <= REL_TOL, f"{what}: max rel err {rel.max():.3e} > {REL_TOL}"
 
 

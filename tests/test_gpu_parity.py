@@ -42,7 +42,7 @@ def test_tiny_full_step():
     out, err = gpu_step(s)
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
-    assert_attention_close(out, ref, "tiny")
+    assert_attention_close(out, ref, "tiny", strict=True)
     # ctx = 1 returns the appended V exactly (fp32 all the way)
     b1 = int(np.where(s.context_lens_np == 1)[0][0])
     for h in range(s.w.H):
@@ -55,7 +55,7 @@ def test_llama2_7b_b8_every_output():
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, "llama2_7b_b8")
+    assert_attention_close(out, ref, "llama2_7b_b8", strict=True)
 
 
 @pytest.mark.parametrize("name,B", [("llama2_13b_b80", 12), ("gqa_skew_b256", 24),
@@ -66,7 +66,7 @@ def test_reduced_batch_every_output(name, B):
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, name)
+    assert_attention_close(out, ref, name, strict=True)
 
 
 def _sample(s, k=10, seed=0):
@@ -85,7 +85,7 @@ def test_full_size_sampled(name):
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out[reqs], ref, name)
+    assert_attention_close(out[reqs], ref, name, strict=True)
     assert torch.isfinite(out.float()).all()
 
 
@@ -153,6 +153,10 @@ def test_empty_and_single_token_histories():
     out, err = gpu_step(s)
     assert err == 0
     assert_attention_close(out, ref, "empty/single")
+    s2 = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=7)
+    out32, err = gpu_step(s2, out_dtype=torch.float32)
+    assert err == 0
+    assert_attention_close(out32, ref, "empty/single, fp32 output")
     assert (out[lens == 0] == 0).all()
     for b in np.where(lens == 1)[0]:
         assert torch.equal(out[b], s.v_new[b].to(out.dtype))  # exact: p = 1
@@ -183,6 +187,10 @@ def test_many_one_block_requests():
     out, err = gpu_step(s)
     assert err == 0
     assert_attention_close(out, ref, "600 one-block requests")
+    s2 = wl.make_step(w, device=DEV, lengths=lens)
+    out32, err = gpu_step(s2, out_dtype=torch.float32)
+    assert err == 0
+    assert_attention_close(out32, ref, "600 one-block requests, fp32 output")
 
 
 def test_unused_rows_poisoned_with_nan_are_never_read():
@@ -204,8 +212,10 @@ def test_shared_prefix_blocks_give_identical_rows():
     s.q[1] = s.q[0]
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert torch.equal(out[0], out[1])
     ref, _, _, _ = oracle_full_step(s, append=False)
+    assert np.array_equal(ref[0], ref[1])
+    # The two rows may be split at different worker boundaries, so they can differ in the
+    # fp32 summation order; both must match the (identical) oracle rows.
     assert_attention_close(out, ref, "shared prefix")
 
 
