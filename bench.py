@@ -387,7 +387,7 @@ def run_ours(args, ws, rank, local):
         sample = oracle_sample(w, args.cpu_seconds, threads)
         sb = step_bytes(sample, sample.pack_requests)
         reps, t_cpu = 0, 0.0
-        while t_cpu < args.cpu_seconds * 0.5 or reps == 0:
+        while t_cpu < args.cpu_seconds or reps == 0:
             t_cpu += oracle_pass(sample, threads)
             reps += 1
         res["cpu_baseline"] = {

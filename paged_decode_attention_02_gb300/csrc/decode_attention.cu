@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     return;
   }
 
+  // The combine grid may be scheduled now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -532,52 +534,85 @@ struct CombineParams {
   int out_bf16;
 };
 
-// One warp per (request, kv-head) segment; merges the pieces of segments that were cut by
-// worker-range boundaries:  M = max m_j,  L = sum l_j 2^(m_j - M),
-// out = sum o_j 2^(m_j - M) / L.
+// One warp per (request, kv-head, query head of the group); merges the pieces of segments
+// cut by worker-range boundaries:  M = max m_j,  L = sum l_j 2^(m_j - M),
+// out = sum o_j 2^(m_j - M) / L. Lanes read the pieces' (m, l) in parallel, then stream the
+// pieces' o rows with all loads of a group of pieces in flight together.
+// Launched as a programmatic dependent of attn_partial_kernel: it may become resident while
+// that grid is still running and waits for its completion (and memory flush) before
+// reading the workspace.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int seg = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (seg >= p.B * p.H_kv) return;
+  const long long gw = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int G = p.G, D = p.D;
+  if (gw >= static_cast<long long>(p.B) * p.H_kv * G) return;
+  const int seg = static_cast<int>(gw / G), j = static_cast<int>(gw % G);
   const int b = seg / p.H_kv, h = seg % p.H_kv;
   const int nb = p.ws_prefix[b + 1] - p.ws_prefix[b];
   if (nb == 0) return;
   const int W = p.ws_prefix[p.B] * p.H_kv;
   const int NW = p.num_workers;
   const int S = p.ws_prefix[b] * p.H_kv + h * nb;
-  const int E = S + nb;
-  const int w0 = tile_owner(S, W, NW), w1 = tile_owner(E - 1, W, NW);
-  if (w0 == w1) return;
+  const int w0 = tile_owner(S, W, NW), w1 = tile_owner(S + nb - 1, W, NW);
+  if (w0 == w1) return;  // written whole by its worker
   const bool w0_tail = S != tile_start(w0, W, NW);
-  const int G = p.G, D = p.D;
-  for (int j = 0; j < G; ++j) {
-    float M = -INFINITY;
-    for (int w = w0; w <= w1; ++w) {
-      if (tile_start(w, W, NW) == tile_start(w + 1, W, NW)) continue;
-      const int slot = 2 * w + ((w == w0 && w0_tail) ? 1 : 0);
-      M = fmaxf(M, p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2]);
+  auto slot_of = [&](int w) { return 2 * w + ((w == w0 && w0_tail) ? 1 : 0); };
+  auto live = [&](int w) { return tile_start(w, W, NW) != tile_start(w + 1, W, NW); };
+
+  // pass 1: M over pieces (lanes in parallel)
+  float M = -INFINITY;
+  for (int w = w0 + lane; w <= w1; w += 32)
+    if (live(w)) M = fmaxf(M, p.ws_ml[(static_cast<size_t>(slot_of(w)) * G + j) * 2]);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, m));
+
+  // pass 2: weights, L, and the weighted sum of o rows
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float Lsum = 0.f;
+  const int per = D / 32;  // 2 or 4 dims per lane
+  for (int base = w0; base <= w1; base += 32) {
+    const int w = base + lane;
+    float f = 0.f;
+    if (w <= w1 && live(w)) {
+      const size_t k = (static_cast<size_t>(slot_of(w)) * G + j) * 2;
+      f = ex2(p.ws_ml[k] - M);
+      Lsum += p.ws_ml[k + 1] * f;
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float Lsum = 0.f;
-    const int per = D / 32;
-    for (int w = w0; w <= w1; ++w) {
-      if (tile_start(w, W, NW) == tile_start(w + 1, W, NW)) continue;
-      const int slot = 2 * w + ((w == w0 && w0_tail) ? 1 : 0);
-      const float m = p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2];
-      const float l = p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1];
-      const float f = ex2(m - M);
-      Lsum += l * f;
-      const float* o = p.ws_o + (static_cast<size_t>(slot) * G + j) * D;
-      for (int e = 0; e < per; ++e) acc[e] += o[lane + 32 * e] * f;
+    const int n = min(32, w1 - base + 1);
+    for (int i = 0; i < n; i += 4) {
+      float fi[4], v[4][4];
+      const float* row[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        fi[u] = __shfl_sync(kFullMask, f, (i + u) & 31);
+        const int wu = base + i + u;
+        row[u] = (i + u < n && fi[u] != 0.f)
+                     ? p.ws_o + (static_cast<size_t>(slot_of(wu)) * G + j) * D
+                     : nullptr;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[u][e] = (row[u] != nullptr && e < per) ? row[u][lane + 32 * e] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(v[u][e], fi[u], acc[e]);
     }
-    const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
-    for (int e = 0; e < per; ++e) {
-      const float v = acc[e] / Lsum;
-      if (p.out_bf16)
-        reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
-      else
-        reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
-    }
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) Lsum += __shfl_xor_sync(kFullMask, Lsum, m);
+  const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (e >= per) break;
+    const float v = acc[e] / Lsum;
+    if (p.out_bf16)
+      reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
+    else
+      reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
   }
 }
 
@@ -762,8 +797,17 @@ extern "C" pda_status pda_paged_decode_attention(
   cp.D = D;
   cp.num_workers = ap.num_workers;
   cp.out_bf16 = ap.out_bf16;
-  const int segs = B * H_kv;
-  attn_combine_kernel<<<(segs + 3) / 4, 128, 0, stream>>>(cp);
-  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  const long long warps = static_cast<long long>(B) * H;  // one per (segment, group head)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, cp) != cudaSuccess) return PDA_ERR_CUDA;
   return PDA_OK;
 }
