@@ -8,7 +8,8 @@
  *
  * Conventions shared by every entry point:
  *  - Every pointer argument is a DEVICE pointer unless its comment says "host". The caller
- *    owns all memory; the library allocates nothing and keeps no per-call state.
+ *    owns all memory; the library allocates nothing. Apart from the fixed scratch array of
+ *    pda_paged_decode_attention_noalloc it keeps no state between calls.
  *  - Tensors are dense and row-major with exactly the shapes given; no strides.
  *  - KV caches are [num_blocks, block_size, H_kv, D]: physical block p holds block_size
  *    consecutive tokens, token row r of block p is at ((p * block_size + r) * H_kv) * D.
@@ -20,9 +21,9 @@
  *    contiguous or ordered, and several requests may share blocks (same page, sec. 2.2
  *    step 2 and sec. 2.3). Entries past a request's last block are never read.
  *  - Query head h reads kv-head h / (H / H_kv) (grouped-query attention, contiguous groups).
- *  - Every call is asynchronous on `stream`, never synchronises the host and makes no
- *    allocation, so a sequence of calls can be captured in a CUDA graph once each kernel
- *    has been launched at least once outside capture.
+ *  - Every call is asynchronous on `stream` and never synchronises the host. Calls other
+ *    than pda_paged_decode_attention_noalloc make no allocation, so a sequence of them can
+ *    be captured in a CUDA graph once each kernel has been launched outside capture.
  *  - Host-checkable errors (null pointers, bad sizes, unsupported dtypes or shapes,
  *    misaligned pointers) return a status before anything is launched. Errors in device
  *    data (a block id or slot out of range, a context length beyond capacity) cannot be
@@ -47,7 +48,8 @@ typedef enum {
   PDA_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size, misalignment */
   PDA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
   PDA_ERR_CUDA = 3,        /* a CUDA runtime call failed; see cudaGetLastError */
-  PDA_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+  PDA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  PDA_ERR_TOO_LARGE = 5    /* needs more scratch than pda_paged_decode_attention_noalloc has */
 } pda_status;
 
 typedef enum { PDA_F32 = 0, PDA_BF16 = 1 } pda_dtype;
@@ -57,6 +59,9 @@ typedef enum { PDA_F32 = 0, PDA_BF16 = 1 } pda_dtype;
 #define PDA_DEVERR_BLOCK_ID 0x2    /* a block id needed by a request is outside [0, num_blocks) */
 #define PDA_DEVERR_SLOT 0x4        /* slot_mapping[b] >= num_blocks * block_size */
 #define PDA_DEVERR_TIMEOUT 0x8     /* a pipeline wait passed its time limit; results invalid */
+
+/* Bytes of the fixed device scratch behind pda_paged_decode_attention_noalloc. */
+#define PDA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* Most requests one batched pack call takes. */
 #define PDA_PACK_MAX_BATCH 64
@@ -146,6 +151,39 @@ pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_ca
                                       pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype,
                                       int sm_cap, void* workspace, size_t workspace_bytes,
                                       int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_paged_decode_attention_noalloc -- pda_paged_decode_attention without a workspace
+ * argument, for callers that cannot allocate device memory.
+ *
+ * The pages describe no such call; it exists for code that may not call cudaMalloc or any
+ * allocator when it runs: a plugin inside a host framework that owns all device memory and
+ * hands out only inputs and outputs, or a serving loop that forbids allocation once it has
+ * started. Such a caller still provides q, the caches, the tables, the lengths and out
+ * exactly as for pda_paged_decode_attention (same meaning, layout and errors); the scratch
+ * the kernels need comes from one fixed array of PDA_NOALLOC_SCRATCH_BYTES bytes compiled
+ * into the library as a device global. Every GPU that loads the library holds that array
+ * until the process exits. The call itself never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *
+ *  - Sizes whose scratch need exceeds PDA_NOALLOC_SCRATCH_BYTES (see
+ *    pda_attention_workspace_size) are rejected with PDA_ERR_TOO_LARGE before any launch.
+ *    On a 152-SM GB300 this admits every supported shape with H / H_kv <= 4 at D = 128
+ *    (about 5 MB) and rejects H / H_kv = 8 at D = 128 (about 10 MB).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *    with that device current) and caches it; make that first call before any stream
+ *    capture on that device.
+ *  - Every call shares the one array, which keeps the previous call's contents. Nothing in
+ *    it needs to start at zero: each call writes every scratch word before reading it.
+ *    Calls that overlap on the GPU (on different streams, or from different host threads)
+ *    race on the array and produce wrong results; serialise them.
+ */
+pda_status pda_paged_decode_attention_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
+    float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
+    int32_t* error_word, cudaStream_t stream);
 
 /*
  * pda_kv_pack_blocks -- gather one request's KV into one contiguous buffer.

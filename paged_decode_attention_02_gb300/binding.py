@@ -15,15 +15,17 @@ import torch
 
 from . import build_lib
 
-PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE = range(5)
+(PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE,
+ PDA_ERR_TOO_LARGE) = range(6)
 PDA_F32, PDA_BF16 = 0, 1
 PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PDA_PACK_MAX_BATCH = 64
+PDA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 EXPORTED = [
     "pda_status_string", "pda_version", "pda_device_sm_count", "pda_kv_append",
     "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
-    "pda_kv_pack_blocks_batched",
+    "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -63,6 +65,9 @@ def load():
         lib.pda_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F,
                                                    I, I, I, I, P, SZ, P, P]
         lib.pda_paged_decode_attention.restype = I
+        lib.pda_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I,
+                                                           I, I, F, I, I, I, I, P, P]
+        lib.pda_paged_decode_attention_noalloc.restype = I
         lib.pda_kv_pack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
         lib.pda_kv_pack_blocks.restype = I
         lib.pda_kv_pack_blocks_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P, P]
@@ -152,6 +157,24 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         _dtype(q), _dtype(k_cache), _dtype(out), int(sm_cap), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
         "pda_paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   max_context_len: int, scale: float, sm_cap: int = 0,
+                                   error_word=None, stream=None):
+    """``paged_decode_attention`` with the library's fixed scratch instead of a workspace,
+    for callers that may not allocate device memory. Calls that overlap on the GPU race."""
+    B, H, D = q.shape
+    NB, bs, H_kv, D2 = k_cache.shape
+    assert D == D2 and v_cache.shape == k_cache.shape and out.shape == q.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    _check(load().pda_paged_decode_attention_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
+        _ptr(context_lens), int(max_context_len), B, H, H_kv, D, bs, NB, float(scale),
+        _dtype(q), _dtype(k_cache), _dtype(out), int(sm_cap), _ptr(error_word),
+        _stream(stream)), "pda_paged_decode_attention_noalloc")
     return out
 
 

@@ -30,7 +30,9 @@
 //    2 * D * sizeof(elem) bytes, far below the tensor-core break-even.
 #include <math.h>
 
+#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "pda_device.cuh"
 #include "pda_internal.h"
@@ -810,4 +812,56 @@ extern "C" pda_status pda_paged_decode_attention(
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, cp) != cudaSuccess) return PDA_ERR_CUDA;
   return PDA_OK;
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch for pda_paged_decode_attention_noalloc: a fixed device array in this module, for
+// callers that cannot allocate. Host code must not pass `g_noalloc_scratch` itself to a
+// kernel (on the host it names a host-side shadow, not device memory); it passes the
+// address cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PDA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::atomic<void*> g_noalloc_ptr[kNoallocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on `dev` (the current device), looked up once.
+pda_status noalloc_scratch(int dev, void** ptr) {
+  if (dev < 0 || dev >= kNoallocMaxDevices) return PDA_ERR_UNSUPPORTED;
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return PDA_ERR_CUDA;
+      g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *ptr = p;
+  return PDA_OK;
+}
+}  // namespace
+
+extern "C" pda_status pda_paged_decode_attention_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
+    float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
+    int32_t* error_word, cudaStream_t stream) {
+  size_t need = 0;
+  pda_status st = pda_attention_workspace_size(B, H, H_kv, D, block_size, kv_dtype, sm_cap,
+                                               &need);
+  if (st != PDA_OK) return st;
+  if (need > PDA_NOALLOC_SCRATCH_BYTES) return PDA_ERR_TOO_LARGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  void* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != PDA_OK) return st;
+  return pda_paged_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    context_lens, max_context_len, B, H, H_kv, D, block_size,
+                                    num_blocks, scale, q_dtype, kv_dtype, out_dtype, sm_cap,
+                                    scratch, PDA_NOALLOC_SCRATCH_BYTES, error_word, stream);
 }

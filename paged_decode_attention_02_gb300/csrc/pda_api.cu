@@ -75,6 +75,7 @@ extern "C" const char* pda_status_string(pda_status status) {
     case PDA_ERR_UNSUPPORTED: return "unsupported shape, dtype or size";
     case PDA_ERR_CUDA: return "CUDA runtime error";
     case PDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PDA_ERR_TOO_LARGE: return "sizes need more scratch than the no-allocation entry point has";
   }
   return "unknown status";
 }
