@@ -39,8 +39,19 @@
 
 namespace pda {
 
+#ifndef PDA_ATTN_WARPS
+#define PDA_ATTN_WARPS 12     // preferred warps (workers) per block
+#endif
+#ifndef PDA_ATTN_MAX_STAGES
+#define PDA_ATTN_MAX_STAGES 4  // most pipeline stages per warp
+#endif
+
 constexpr int kBS = 16;             // tokens per physical block (box height of the TMA)
-constexpr int kMaxWarps = 8;        // warps (workers) per block
+constexpr int kMaxWarps = PDA_ATTN_WARPS;
+// Warps per block for a GQA group of G: the group of 8 keeps 8 warps so its 8 heads of q
+// and o stay in registers (up to 255 per thread).
+__host__ __device__ constexpr int warps_for_group(int G) { return G >= 8 ? 8 : kMaxWarps; }
+constexpr int kMetaBytesPerWarp = 2 * 32 * 8;  // two groups of 32 (block id, length) pairs
 constexpr int kMaxBatch = 8192;     // prefix table size bound (shared memory)
 constexpr int kSmemBudget = 226 * 1024;  // dynamic bytes; static shared memory sits on top
 constexpr int kMinResidentSmem = 116 * 1024;  // > half an SM: never two blocks per SM
@@ -73,26 +84,23 @@ __host__ __device__ __forceinline__ int tile_owner(int t, int W, int NW) {
 }
 
 // Reduce-scatter over the lanes of one row group: n values per lane, xor masks from
-// `mask` down to 1. While n > 1 each step keeps half of the values (the upper half on
-// lanes whose mask bit is set) and adds the partner's copy of that half; once one value
-// is left the remaining steps are plain butterflies.
+// `mask` down to 1. While n > 1 every lane keeps the lower half of its values and adds the
+// partner's upper half; once one value is left the remaining steps are plain butterflies.
+// This leaves each lane with complete sums only because every lane stores its values in a
+// lane-dependent order (see WarpAttn::init): local index u holds real index u ^ idx0, so a
+// lane's lower half is exactly the half its partner sends it.
 template <int n, int mask>
 struct ReduceScatter {
-  static __device__ __forceinline__ void run(float* v, int lane) {
+  static __device__ __forceinline__ void run(float* v) {
     if constexpr (mask == 0) {
       return;
     } else if constexpr (n > 1) {
-      const bool upper = (lane & mask) != 0;
 #pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        const float keep = upper ? v[i + n / 2] : v[i];
-        const float send = upper ? v[i] : v[i + n / 2];
-        v[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
-      }
-      ReduceScatter<n / 2, mask / 2>::run(v, lane);
+      for (int i = 0; i < n / 2; ++i) v[i] += __shfl_xor_sync(kFullMask, v[i + n / 2], mask);
+      ReduceScatter<n / 2, mask / 2>::run(v);
     } else {
       v[0] += __shfl_xor_sync(kFullMask, v[0], mask);
-      ReduceScatter<1, mask / 2>::run(v, lane);
+      ReduceScatter<1, mask / 2>::run(v);
     }
   }
 };
@@ -108,24 +116,37 @@ struct Geometry {
   static constexpr int C = N >= LPR ? N / LPR : 1;  // complete scores per lane
   static constexpr int DUP = N >= LPR ? 1 : LPR / N;  // lanes holding the same score
   static constexpr int LPH = N >= LPR ? LPR / G : LPR;  // lanes of a row group per head
+  // Scores of two token slots share one packed fp32x2 FMA when q fits twice in registers.
+  static constexpr bool PAIR_QK = G * VEC <= 32 && TPL % 2 == 0;
   static constexpr uint32_t TILE_BYTES = kBS * D * sizeof(KV);
   static constexpr uint32_t Q_BYTES = G * D * sizeof(KV);
   static_assert(32 % LPR == 0 && kBS % RPW == 0, "row geometry");
   static_assert(LPR >= G, "one head per lane after the reduce-scatter");
+  static_assert(VEC % 2 == 0, "packed fp32x2 accumulation");
   static_assert(TILE_BYTES % 128 == 0 && Q_BYTES % 16 == 0, "smem alignment");
 };
 
 // Per-warp online-softmax state and tile arithmetic.
+//
+// Lane layout: lane = rw * LPR + cl; the lane covers dims [cl*VEC, cl*VEC + VEC) of the
+// rows rw, rw + RPW, ... (token slot i is row rw + RPW * i of the 16-row tile). Each lane
+// forms N = G * TPL partial dot products (head j, slot i; real index j * TPL + i), sums
+// them with the other lanes of its row group by a reduce-scatter, and is left with C
+// complete scores of one head: real indices idx0 .. idx0 + C - 1.
 template <typename KV, int D, int G>
 struct WarpAttn {
   using Geo = Geometry<KV, D, G>;
   using E = typename Geo::E;
   static constexpr int VEC = Geo::VEC, LPR = Geo::LPR, RPW = Geo::RPW, TPL = Geo::TPL;
   static constexpr int N = Geo::N, C = Geo::C, DUP = Geo::DUP, LPH = Geo::LPH;
+  static constexpr bool PAIR_QK = Geo::PAIR_QK;
 
   int lane, rw, cl, idx0;
-  float qr[G][VEC];
-  float o[G][VEC];
+  int hp;             // local head jl holds real head jl ^ hp
+  int krow[TPL];      // element offset of the K row behind local slot il (real slot il ^ tp)
+  float2 q2[PAIR_QK ? G : 1][PAIR_QK ? VEC : 1];  // q (scaled), duplicated, local head order
+  float qs[PAIR_QK ? 1 : G][PAIR_QK ? 1 : VEC];   // q (scaled), local head order
+  float2 o2[G][VEC / 2];  // unnormalised output, real head order, dims pairs
   float m_own;  // running max of this lane's head (log2 domain)
   float l_own;  // this lane's share of the running sum of its head
 
@@ -134,42 +155,72 @@ struct WarpAttn {
     rw = lane / LPR;
     cl = lane % LPR;
     idx0 = (cl / DUP) * C;
+    hp = idx0 / TPL;
+    const int tp = idx0 % TPL;
+#pragma unroll
+    for (int il = 0; il < TPL; ++il) krow[il] = (rw + RPW * (il ^ tp)) * D + cl * VEC;
   }
 
   __device__ __forceinline__ void reset(const KV* q_smem, float scale_log2) {
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
+    for (int jl = 0; jl < G; ++jl) {
       float t[VEC];
-      E::load16(q_smem + j * D + cl * VEC, t);
+      E::load16(q_smem + (jl ^ hp) * D + cl * VEC, t);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        qr[j][e] = t[e] * scale_log2;
-        o[j][e] = 0.f;
+        const float qv = t[e] * scale_log2;
+        if constexpr (PAIR_QK)
+          q2[jl][e] = make_float2(qv, qv);
+        else
+          qs[jl][e] = qv;
       }
     }
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) o2[j][e] = make_float2(0.f, 0.f);
     m_own = -INFINITY;
     l_own = 0.f;
   }
 
   template <bool kPartial>
   __device__ __forceinline__ void tile(const KV* ks, const KV* vs, int n_valid) {
+    // ---- scores: part[jl * TPL + il] = q(real head jl ^ hp) . K(real slot il ^ tp)
     float part[N];
+    if constexpr (PAIR_QK) {
 #pragma unroll
-    for (int i = 0; i < TPL; ++i) {
-      const int t = rw + RPW * i;
-      float k[VEC];
-      E::load16(ks + t * D + cl * VEC, k);
+      for (int m = 0; m < TPL / 2; ++m) {
+        float k0[VEC], k1[VEC];
+        E::load16(ks + krow[2 * m], k0);
+        E::load16(ks + krow[2 * m + 1], k1);
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float acc = qr[j][0] * k[0];
+        for (int jl = 0; jl < G; ++jl) {
+          float2 acc = __fmul2_rn(q2[jl][0], make_float2(k0[0], k1[0]));
 #pragma unroll
-        for (int e = 1; e < VEC; ++e) acc = fmaf(qr[j][e], k[e], acc);
-        part[j * TPL + i] = acc;
+          for (int e = 1; e < VEC; ++e)
+            acc = __ffma2_rn(q2[jl][e], make_float2(k0[e], k1[e]), acc);
+          part[jl * TPL + 2 * m] = acc.x;
+          part[jl * TPL + 2 * m + 1] = acc.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int il = 0; il < TPL; ++il) {
+        float k[VEC];
+        E::load16(ks + krow[il], k);
+#pragma unroll
+        for (int jl = 0; jl < G; ++jl) {
+          float acc = qs[jl][0] * k[0];
+#pragma unroll
+          for (int e = 1; e < VEC; ++e) acc = fmaf(qs[jl][e], k[e], acc);
+          part[jl * TPL + il] = acc;
+        }
       }
     }
-    ReduceScatter<N, LPR / 2>::run(part, lane);
+    ReduceScatter<N, LPR / 2>::run(part);
 
-    // part[0..C) are now complete scores of (head idx/TPL, slot idx%TPL), idx = idx0 + r.
+    // part[0..C) are now complete scores of real index idx0 + r: head (idx0 + r) / TPL,
+    // slot (idx0 + r) % TPL.
     float tmax = -INFINITY;
 #pragma unroll
     for (int r = 0; r < C; ++r) {
@@ -199,10 +250,12 @@ struct WarpAttn {
 #pragma unroll
     for (int j = 0; j < G; ++j) {
       const float a = (G == 1) ? alpha : __shfl_sync(kFullMask, alpha, j * LPH);
+      const float2 a2 = make_float2(a, a);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) o[j][e] *= a;
+      for (int e = 0; e < VEC / 2; ++e) o2[j][e] = __fmul2_rn(o2[j][e], a2);
     }
 
+    // ---- o[j] += p(j, slot i) * V(row of slot i), real order
 #pragma unroll
     for (int i = 0; i < TPL; ++i) {
       const int t = rw + RPW * i;
@@ -217,8 +270,10 @@ struct WarpAttn {
         const int idx = j * TPL + i;
         const int src = rw * LPR + (idx / C) * DUP;
         const float p = __shfl_sync(kFullMask, part[idx % C], src);
+        const float2 p2 = make_float2(p, p);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[j][e] = fmaf(p, v[e], o[j][e]);
+        for (int e = 0; e < VEC / 2; ++e)
+          o2[j][e] = __ffma2_rn(p2, make_float2(v[2 * e], v[2 * e + 1]), o2[j][e]);
       }
     }
   }
@@ -234,13 +289,19 @@ struct WarpAttn {
 #pragma unroll
     for (int j = 0; j < G; ++j) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e)
+      for (int e = 0; e < VEC / 2; ++e)
 #pragma unroll
-        for (int mask = LPR; mask < 32; mask <<= 1)
-          o[j][e] += __shfl_xor_sync(kFullMask, o[j][e], mask);
+        for (int mask = LPR; mask < 32; mask <<= 1) {
+          o2[j][e].x += __shfl_xor_sync(kFullMask, o2[j][e].x, mask);
+          o2[j][e].y += __shfl_xor_sync(kFullMask, o2[j][e].y, mask);
+        }
       lj[j] = __shfl_sync(kFullMask, l, j * LPH);
       mj[j] = __shfl_sync(kFullMask, m_own, j * LPH);
     }
+  }
+
+  __device__ __forceinline__ float o(int j, int e) const {
+    return (e & 1) ? o2[j][e >> 1].y : o2[j][e >> 1].x;
   }
 };
 
@@ -270,7 +331,7 @@ __device__ __forceinline__ void store_out(void* out, size_t off, const float* v,
 }
 
 template <typename KV, int D, int G>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+__global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Geo = Geometry<KV, D, G>;
@@ -281,8 +342,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     return;
   }
 
-  // The combine grid may be scheduled now; it waits for this grid to finish.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -295,6 +354,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   const size_t stage_region = static_cast<size_t>(nwarps) * p.stages * p.stage_bytes;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_stage + stage_region);
   int32_t* s_info = reinterpret_cast<int32_t*>(s_bar + nwarps * p.stages);
+  int2* s_meta = reinterpret_cast<int2*>(
+      (reinterpret_cast<uintptr_t>(s_info + nwarps * p.stages) + 7) & ~uintptr_t(7));
 
   // ---- 1. block prefix sums of per-request tile counts (every block computes its own)
   const int cap_tokens = min(p.max_blocks * kBS, p.max_context_len);
@@ -393,35 +454,55 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
   }
   const uint64_t policy = l2_policy_evict_first();
 
-  // Issue-side metadata: lane i describes tile g_base + i.
-  int g_base = -0x40000000;
-  int g_b = 0, g_h = 0, g_blk = 0, g_pid = 0, g_len = 0;
-  auto load_group = [&](int base) {
-    g_base = base;
+  // Issue-side metadata, one group of 32 tiles at a time: lane i describes tile
+  // g_base + i. The block id and context length of the next group are fetched with
+  // cp.async a whole group ahead into this warp's two-slot ring, so the lane that issues a
+  // tile never waits on a global load. Each lane reads only the slot it filled itself.
+  int2* my_meta = s_meta + warp * 64;
+  int g_base = t_begin, g_buf = 0;
+  int cur_b = 0, cur_h = 0, cur_blk = 0, cur_pid = 0, cur_len = 0;
+  int nxt_b = 0, nxt_h = 0, nxt_blk = 0;
+  auto prefetch = [&](int base, int buf) {
     const int y = base + lane;
     if (y < t_end) {
       int nb;
-      locate(y, g_b, g_h, g_blk, nb);
-      g_pid = p.block_tables[static_cast<size_t>(g_b) * p.max_blocks + g_blk];
-      g_len = p.context_lens[g_b];
+      locate(y, nxt_b, nxt_h, nxt_blk, nb);
+      cp_async4(&my_meta[buf * 32 + lane].x,
+                p.block_tables + static_cast<size_t>(nxt_b) * p.max_blocks + nxt_blk);
+      cp_async4(&my_meta[buf * 32 + lane].y, p.context_lens + nxt_b);
     }
+    cp_async_commit();
   };
+  auto enter = [&](int base, int buf) {  // the group starting at `base` becomes current
+    cp_async_wait_all();
+    g_base = base;
+    g_buf = buf;
+    cur_b = nxt_b;
+    cur_h = nxt_h;
+    cur_blk = nxt_blk;
+    const int2 m = my_meta[buf * 32 + lane];
+    cur_pid = m.x;
+    cur_len = m.y;
+    if (base + 32 < t_end) prefetch(base + 32, buf ^ 1);
+  };
+  prefetch(t_begin, 0);
+  enter(t_begin, 0);
   auto issue = [&](int x, int s) {
-    if (x >= g_base + 32) load_group(x);
+    if (x >= g_base + 32) enter(g_base + 32, g_buf ^ 1);
     if (lane == x - g_base) {
-      const bool bad = g_pid < 0 || g_pid >= p.num_blocks;
-      const bool need_q = (g_blk == 0) || (x == t_begin);
-      const int n_valid = min(kBS, g_len - g_blk * kBS);
+      const bool bad = cur_pid < 0 || cur_pid >= p.num_blocks;
+      const bool need_q = (cur_blk == 0) || (x == t_begin);
+      const int n_valid = min(kBS, cur_len - cur_blk * kBS);
       my_info[s] = n_valid | (bad ? 0x100 : 0);
       if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
       const uint32_t bytes = 2 * Geo::TILE_BYTES + (need_q ? Geo::Q_BYTES : 0);
       mbar_arrive_expect_tx(&my_bar[s], bytes);
-      const int row = (bad ? 0 : g_pid) * kBS;
-      tma_load_3d(k_buf(s), &tmK, 0, g_h, row, &my_bar[s], policy);
-      tma_load_3d(v_buf(s), &tmV, 0, g_h, row, &my_bar[s], policy);
+      const int row = (bad ? 0 : cur_pid) * kBS;
+      tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
+      tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
       if (need_q) {
         const KV* src = reinterpret_cast<const KV*>(p.q) +
-                        (static_cast<size_t>(g_b) * p.H + static_cast<size_t>(g_h) * G) * D;
+                        (static_cast<size_t>(cur_b) * p.H + static_cast<size_t>(cur_h) * G) * D;
         bulk_load(q_buf(s), src, Geo::Q_BYTES, &my_bar[s]);
       }
     }
@@ -444,6 +525,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&my_bar[stage], phase));
     if (!ready) {
       atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
+      cp_async_wait_all();
       // Give copies still in flight a bounded chance to land before leaving.
       for (int y = x; y < min(t_end, x + S); ++y) {
         const int s2 = (stage + (y - x)) % S;
@@ -488,7 +570,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             float v[W::VEC];
             const float inv = seg_bad ? __int_as_float(0x7fc00000) : 1.f / lj[j];
 #pragma unroll
-            for (int e = 0; e < W::VEC; ++e) v[e] = st.o[j][e] * inv;
+            for (int e = 0; e < W::VEC; ++e) v[e] = st.o(j, e) * inv;
             const size_t off =
                 (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D +
                 st.cl * W::VEC;
@@ -502,7 +584,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < W::VEC; e += 4)
               *reinterpret_cast<float4*>(dst + e) =
-                  make_float4(st.o[j][e], st.o[j][e + 1], st.o[j][e + 2], st.o[j][e + 3]);
+                  make_float4(st.o(j, e), st.o(j, e + 1), st.o(j, e + 2), st.o(j, e + 3));
             if (st.cl == 0) {
               p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
               p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
@@ -524,6 +606,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
       if (cb < B) cnb = s_pre[cb + 1] - s_pre[cb];
     }
   }
+  // This warp's work is done: the combine grid may be scheduled (it still waits for the
+  // whole grid to finish before reading the workspace).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 struct CombineParams {
@@ -637,20 +722,23 @@ uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
 bool make_plan(int B, int G, int D, pda_dtype kv, int sm_cap, int num_sms, LaunchPlan* pl) {
   pl->stage_bytes = stage_bytes_for(kv, D, G);
   pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, 128));
+  const size_t fixed = pl->prefix_bytes + 8;  // + alignment of the metadata ring
+  if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
   pl->nwarps = 0;
-  for (int nw = kMaxWarps; nw >= 2; nw /= 2) {
-    const size_t fixed = pl->prefix_bytes;
+  // The most warps that still get two stages each; then as many stages as fit.
+  for (int nw = warps_for_group(G); nw >= 2; --nw) {
     const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
-    if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
-    const int stages = static_cast<int>((kSmemBudget - fixed) / per_stage);
+    const size_t meta = static_cast<size_t>(nw) * kMetaBytesPerWarp;
+    if (fixed + meta >= static_cast<size_t>(kSmemBudget)) continue;
+    const int stages = static_cast<int>((kSmemBudget - fixed - meta) / per_stage);
     if (stages >= 2) {
       pl->nwarps = nw;
-      pl->stages = stages > 4 ? 4 : stages;
+      pl->stages = stages > PDA_ATTN_MAX_STAGES ? PDA_ATTN_MAX_STAGES : stages;
       break;
     }
   }
   if (pl->nwarps == 0) return false;
-  size_t smem = pl->prefix_bytes +
+  size_t smem = fixed + static_cast<size_t>(pl->nwarps) * kMetaBytesPerWarp +
                 static_cast<size_t>(pl->nwarps) * pl->stages * (pl->stage_bytes + 8 + 4);
   smem = round_up(smem, 128);
   if (smem < static_cast<size_t>(kMinResidentSmem)) smem = kMinResidentSmem;
