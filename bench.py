@@ -177,7 +177,7 @@ class L2Flush:
     def __call__(self):
         import torch
         self.w.zero_()
-        torch.sum(self.r, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 # ------------------------------------------------------------------ distributed

@@ -138,8 +138,11 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  *                 attention sharing the GPU with other work on a fraction of its SMs
  *                 (review of "Injecting Adrenaline into LLM Serving", sec. 3.3).
  *  workspace      device scratch of at least pda_attention_workspace_size(...) bytes,
- *                 256-byte aligned; no initialisation needed; not shared by calls that
- *                 may run concurrently.
+ *                 256-byte aligned; not shared by calls that may run concurrently. No
+ *                 initialisation is needed: its arrival counters are tagged with a number
+ *                 the library gives each call. (A call captured in a CUDA graph keeps its
+ *                 number on every replay; if a replay ever reports PDA_DEVERR_TIMEOUT, zero
+ *                 the workspace before the next replay.)
  *  Supported: D in {64, 128}, block_size == 16, H / H_kv in {1, 2, 4, 8}, B <= 8192,
  *  kv_dtype in {PDA_F32, PDA_BF16}. Pointers 16-byte aligned.
  */
@@ -174,7 +177,9 @@ pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_ca
  *    with that device current) and caches it; make that first call before any stream
  *    capture on that device.
  *  - Every call shares the one array, which keeps the previous call's contents. Nothing in
- *    it needs to start at zero: each call writes every scratch word before reading it.
+ *    it needs to start at zero: partial results are written before they are read, and the
+ *    per-segment arrival counters carry the number of the call that last wrote them, so
+ *    values left by an earlier call are recognised as stale.
  *    Calls that overlap on the GPU (on different streams, or from different host threads)
  *    race on the array and produce wrong results; serialise them.
  */

@@ -23,9 +23,10 @@
 //    scores. Softmax is online, in base 2 (q is pre-scaled by scale * log2 e).
 //  * A segment that lies wholly inside one worker's range is normalised and written
 //    directly. A segment cut by a range boundary leaves (m, l, o) pieces in the workspace
-//    (at most two per worker), merged by attn_combine_kernel with a log-sum-exp combine:
-//    the split and merge of Orca's iteration-level batching (page "Disaggregated LLM
-//    Serving", sec. 2.1), applied along the sequence.
+//    (at most two per worker); the warp that registers a segment's last piece merges them
+//    with a log-sum-exp combine, so no second kernel is needed. This is the split and merge
+//    of Orca's iteration-level batching (page "Disaggregated LLM Serving", sec. 2.1),
+//    applied along the sequence.
 //  * No tensor cores: per kv-head and token this is G dot products of length D against
 //    2 * D * sizeof(elem) bytes, far below the tensor-core break-even.
 #include <math.h>
@@ -61,9 +62,10 @@ struct AttnParams {
   const void* q;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* ws_o;         // [2 * num_workers][G][D]
-  float* ws_ml;        // [2 * num_workers][G][2]
-  int32_t* ws_prefix;  // [B + 1] block prefix sums, for the combine kernel
+  float* ws_o;                    // [2 * num_workers][G][D]   piece outputs
+  float* ws_ml;                   // [2 * num_workers][G][2]   piece (max, sum)
+  unsigned long long* ws_arrive;  // [B * H_kv] piece arrivals: call number << 16 | count
+  unsigned long long call;        // this call's number (48 bits)
   int32_t* error_word;
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
   int out_bf16;
@@ -330,6 +332,87 @@ __device__ __forceinline__ void store_out(void* out, size_t off, const float* v,
   }
 }
 
+// Registers one more piece of a segment and returns how many pieces of it this call has
+// registered so far. The counter holds (call number << 16) | count; a counter written by
+// an earlier call (or one that was aborted) carries another call number and counts as 0.
+__device__ __forceinline__ unsigned arrive(unsigned long long* counter,
+                                           unsigned long long call) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+  while (true) {
+    const unsigned long long next = ((old >> 16) == call) ? old + 1 : ((call << 16) | 1ull);
+    const unsigned long long seen = atomicCAS(counter, old, next);
+    if (seen == old) return static_cast<unsigned>(next & 0xffffull);
+    old = seen;
+  }
+}
+
+// Log-sum-exp merge of the pieces of one segment (request b, kv-head h) into out, done by
+// the warp that registered the segment's last piece. Pieces come from workers w0..w1 (the
+// first may hold it as its tail piece); empty workers hold none. For each head j:
+//   M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum o_i 2^(m_i - M) / L.
+// Pieces are read from L2 (ld.cg): other SMs wrote them during this launch.
+template <int D, int G>
+__device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1, bool w0_tail,
+                              int W_tiles, int NW, int lane) {
+  constexpr int PER = D / 32;
+  auto slot_of = [&](int w) { return 2 * w + ((w == w0 && w0_tail) ? 1 : 0); };
+  auto live = [&](int w) {
+    return tile_start(w, W_tiles, NW) != tile_start(w + 1, W_tiles, NW);
+  };
+#pragma unroll 1
+  for (int j = 0; j < G; ++j) {
+    float M = -INFINITY;
+    for (int w = w0 + lane; w <= w1; w += 32)
+      if (live(w)) M = fmaxf(M, __ldcg(p.ws_ml + (static_cast<size_t>(slot_of(w)) * G + j) * 2));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, m));
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float Lsum = 0.f;
+    for (int base = w0; base <= w1; base += 32) {
+      const int w = base + lane;
+      float f = 0.f;
+      if (w <= w1 && live(w)) {
+        const size_t k = (static_cast<size_t>(slot_of(w)) * G + j) * 2;
+        f = ex2(__ldcg(p.ws_ml + k) - M);
+        Lsum += __ldcg(p.ws_ml + k + 1) * f;
+      }
+      const int n = min(32, w1 - base + 1);
+      for (int i = 0; i < n; i += 4) {
+        float fi[4], v[4][PER];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          fi[u] = __shfl_sync(kFullMask, f, (i + u) & 31);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+          if (i + u < n && fi[u] != 0.f) {
+            const float* row =
+                p.ws_o + (static_cast<size_t>(slot_of(base + i + u)) * G + j) * D;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) v[u][e] = __ldcg(row + lane + 32 * e);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(v[u][e], fi[u], acc[e]);
+      }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) Lsum += __shfl_xor_sync(kFullMask, Lsum, m);
+    const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const float v = acc[e] / Lsum;
+      if (p.out_bf16)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
+      else
+        reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
+    }
+  }
+}
+
 template <typename KV, int D, int G>
 __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -411,8 +494,6 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
         reinterpret_cast<float*>(p.out)[off] = val;
     }
   }
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= B; i += blockDim.x) p.ws_prefix[i] = s_pre[i];
 
   // ---- 3. this warp's tile range
   const int H_kv = p.H_kv;
@@ -563,8 +644,8 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
       const int seg_start = s_pre[cb] * H_kv + ch * cnb;
       const int seg_end = seg_start + cnb;
       const bool complete = seg_start >= t_begin && seg_end <= t_end;
-      if (st.rw == 0) {
-        if (complete) {
+      if (complete) {
+        if (st.rw == 0) {
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             float v[W::VEC];
@@ -576,8 +657,12 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
                 st.cl * W::VEC;
             store_out(p.out, off, v, W::VEC, p.out_bf16);
           }
-        } else {
-          const int slot = 2 * w + (seg_start <= t_begin ? 0 : 1);
+        }
+      } else {
+        // A piece of a segment cut by a range boundary: store (m, l, o), register it, and
+        // merge the segment if this was its last piece.
+        const int slot = 2 * w + (seg_start <= t_begin ? 0 : 1);
+        if (st.rw == 0) {
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             float* dst = p.ws_o + (static_cast<size_t>(slot) * G + j) * D + st.cl * W::VEC;
@@ -591,6 +676,26 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
                   seg_bad ? __int_as_float(0x7fc00000) : lj[j];
             }
           }
+        }
+        __threadfence();  // this lane's piece stores before the arrival below
+        __syncwarp();
+        const int seg = cb * H_kv + ch;
+        unsigned arrived = 0;
+        if (lane == 0) arrived = arrive(p.ws_arrive + seg, p.call);
+        arrived = __shfl_sync(kFullMask, arrived, 0);
+        const int w0 = tile_owner(seg_start, W_tiles, NW);
+        const int w1 = tile_owner(seg_end - 1, W_tiles, NW);
+        unsigned pieces = 0;
+        for (int wb = w0; wb <= w1; wb += 32) {
+          const int ww = wb + lane;
+          const bool has = ww <= w1 && tile_start(ww, W_tiles, NW) != tile_start(ww + 1, W_tiles, NW);
+          pieces += __popc(__ballot_sync(kFullMask, has));
+        }
+        if (arrived == pieces) {
+          __threadfence();  // see the other pieces' stores
+          merge_segment<D, G>(p, cb, ch, w0, w1, seg_start != tile_start(w0, W_tiles, NW),
+                              W_tiles, NW, lane);
+          if (lane == 0) atomicExch(p.ws_arrive + seg, p.call << 16);
         }
       }
     }
@@ -606,101 +711,6 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
       if (cb < B) cnb = s_pre[cb + 1] - s_pre[cb];
     }
   }
-  // This warp's work is done: the combine grid may be scheduled (it still waits for the
-  // whole grid to finish before reading the workspace).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-struct CombineParams {
-  void* out;
-  const float* ws_o;
-  const float* ws_ml;
-  const int32_t* ws_prefix;
-  int B, H, H_kv, G, D;
-  int num_workers;
-  int out_bf16;
-};
-
-// One warp per (request, kv-head, query head of the group); merges the pieces of segments
-// cut by worker-range boundaries:  M = max m_j,  L = sum l_j 2^(m_j - M),
-// out = sum o_j 2^(m_j - M) / L. Lanes read the pieces' (m, l) in parallel, then stream the
-// pieces' o rows with all loads of a group of pieces in flight together.
-// Launched as a programmatic dependent of attn_partial_kernel: it may become resident while
-// that grid is still running and waits for its completion (and memory flush) before
-// reading the workspace.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long long gw = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  const int G = p.G, D = p.D;
-  if (gw >= static_cast<long long>(p.B) * p.H_kv * G) return;
-  const int seg = static_cast<int>(gw / G), j = static_cast<int>(gw % G);
-  const int b = seg / p.H_kv, h = seg % p.H_kv;
-  const int nb = p.ws_prefix[b + 1] - p.ws_prefix[b];
-  if (nb == 0) return;
-  const int W = p.ws_prefix[p.B] * p.H_kv;
-  const int NW = p.num_workers;
-  const int S = p.ws_prefix[b] * p.H_kv + h * nb;
-  const int w0 = tile_owner(S, W, NW), w1 = tile_owner(S + nb - 1, W, NW);
-  if (w0 == w1) return;  // written whole by its worker
-  const bool w0_tail = S != tile_start(w0, W, NW);
-  auto slot_of = [&](int w) { return 2 * w + ((w == w0 && w0_tail) ? 1 : 0); };
-  auto live = [&](int w) { return tile_start(w, W, NW) != tile_start(w + 1, W, NW); };
-
-  // pass 1: M over pieces (lanes in parallel)
-  float M = -INFINITY;
-  for (int w = w0 + lane; w <= w1; w += 32)
-    if (live(w)) M = fmaxf(M, p.ws_ml[(static_cast<size_t>(slot_of(w)) * G + j) * 2]);
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, m));
-
-  // pass 2: weights, L, and the weighted sum of o rows
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float Lsum = 0.f;
-  const int per = D / 32;  // 2 or 4 dims per lane
-  for (int base = w0; base <= w1; base += 32) {
-    const int w = base + lane;
-    float f = 0.f;
-    if (w <= w1 && live(w)) {
-      const size_t k = (static_cast<size_t>(slot_of(w)) * G + j) * 2;
-      f = ex2(p.ws_ml[k] - M);
-      Lsum += p.ws_ml[k + 1] * f;
-    }
-    const int n = min(32, w1 - base + 1);
-    for (int i = 0; i < n; i += 4) {
-      float fi[4], v[4][4];
-      const float* row[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        fi[u] = __shfl_sync(kFullMask, f, (i + u) & 31);
-        const int wu = base + i + u;
-        row[u] = (i + u < n && fi[u] != 0.f)
-                     ? p.ws_o + (static_cast<size_t>(slot_of(wu)) * G + j) * D
-                     : nullptr;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          v[u][e] = (row[u] != nullptr && e < per) ? row[u][lane + 32 * e] : 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = fmaf(v[u][e], fi[u], acc[e]);
-    }
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) Lsum += __shfl_xor_sync(kFullMask, Lsum, m);
-  const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (e >= per) break;
-    const float v = acc[e] / Lsum;
-    if (p.out_bf16)
-      reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
-    else
-      reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
-  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -710,7 +720,7 @@ struct LaunchPlan {
   int nwarps, stages, grid;
   uint32_t stage_bytes, prefix_bytes;
   size_t smem_bytes;
-  size_t ws_prefix, ws_ml, ws_o, ws_total;  // byte offsets / total
+  size_t ws_arrive, ws_ml, ws_o, ws_total;  // byte offsets / total
 };
 
 uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
@@ -719,7 +729,8 @@ uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
   return 2 * tile + static_cast<uint32_t>(round_up(static_cast<size_t>(G) * D * e, 128));
 }
 
-bool make_plan(int B, int G, int D, pda_dtype kv, int sm_cap, int num_sms, LaunchPlan* pl) {
+bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
+               LaunchPlan* pl) {
   pl->stage_bytes = stage_bytes_for(kv, D, G);
   pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, 128));
   const size_t fixed = pl->prefix_bytes + 8;  // + alignment of the metadata ring
@@ -747,8 +758,8 @@ bool make_plan(int B, int G, int D, pda_dtype kv, int sm_cap, int num_sms, Launc
   if (sm_cap > 0 && sm_cap < grid) grid = sm_cap;
   pl->grid = grid;
   const size_t nw_total = static_cast<size_t>(grid) * pl->nwarps;
-  pl->ws_prefix = 0;
-  pl->ws_ml = round_up(static_cast<size_t>(B + 1) * 4, 256);
+  pl->ws_arrive = 0;
+  pl->ws_ml = round_up(static_cast<size_t>(B) * H_kv * 8, 256);
   pl->ws_o = pl->ws_ml + round_up(2 * nw_total * G * 2 * 4, 256);
   pl->ws_total = pl->ws_o + round_up(2 * nw_total * G * static_cast<size_t>(D) * 4, 256);
   return true;
@@ -780,6 +791,9 @@ KernelFn pick_kernel(pda_dtype kv, int D, int G) {
 
 bool supported_g(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 
+// Numbers the calls, so a call recognises arrival counters left by earlier ones.
+std::atomic<unsigned long long> g_call{1};
+
 }  // namespace
 }  // namespace pda
 
@@ -797,7 +811,7 @@ extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D
   const pda_status st = current_device_sms(&dev, &sms);
   if (st != PDA_OK) return st;
   LaunchPlan pl;
-  if (!make_plan(B, H / H_kv, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  if (!make_plan(B, H_kv, H / H_kv, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
   *bytes = pl.ws_total;
   return PDA_OK;
 }
@@ -833,7 +847,7 @@ extern "C" pda_status pda_paged_decode_attention(
   pda_status st = current_device_sms(&dev, &sms);
   if (st != PDA_OK) return st;
   LaunchPlan pl;
-  if (!make_plan(B, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  if (!make_plan(B, H_kv, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
   if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
 
   KernelFn fn = pick_kernel(kv_dtype, D, G);
@@ -855,7 +869,8 @@ extern "C" pda_status pda_paged_decode_attention(
   ap.q = q;
   ap.block_tables = block_tables;
   ap.context_lens = context_lens;
-  ap.ws_prefix = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
+  ap.ws_arrive = reinterpret_cast<unsigned long long*>(ws + pl.ws_arrive);
+  ap.call = g_call.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1);
   ap.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   ap.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
   ap.error_word = error_word;
@@ -875,30 +890,6 @@ extern "C" pda_status pda_paged_decode_attention(
   fn<<<pl.grid, pl.nwarps * 32, pl.smem_bytes, stream>>>(tmK, tmV, ap);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
 
-  CombineParams cp;
-  cp.out = out;
-  cp.ws_o = ap.ws_o;
-  cp.ws_ml = ap.ws_ml;
-  cp.ws_prefix = ap.ws_prefix;
-  cp.B = B;
-  cp.H = H;
-  cp.H_kv = H_kv;
-  cp.G = G;
-  cp.D = D;
-  cp.num_workers = ap.num_workers;
-  cp.out_bf16 = ap.out_bf16;
-  const long long warps = static_cast<long long>(B) * H;  // one per (segment, group head)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((warps + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, cp) != cudaSuccess) return PDA_ERR_CUDA;
   return PDA_OK;
 }
 
