@@ -350,67 +350,99 @@ __device__ __forceinline__ unsigned arrive(unsigned long long* counter,
 // the warp that registered the segment's last piece. Pieces come from workers w0..w1 (the
 // first may hold it as its tail piece); empty workers hold none. For each head j:
 //   M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum o_i 2^(m_i - M) / L.
-// Pieces are read from L2 (ld.cg): other SMs wrote them during this launch.
-template <int D, int G>
-__device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1, bool w0_tail,
-                              int W_tiles, int NW, int lane) {
+// All heads are merged together so the loads of one pass are in flight at once: lane i
+// reads piece i's (m, l) of every head, then lanes stream the pieces' o rows. Pieces are
+// read from L2 (ld.cg): other SMs wrote them during this launch.
+template <int D, int G, int HP>
+__device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, int j0, int w0,
+                                            int w1, bool w0_tail, int W_tiles, int NW,
+                                            int lane) {
   constexpr int PER = D / 32;
   auto slot_of = [&](int w) { return 2 * w + ((w == w0 && w0_tail) ? 1 : 0); };
   auto live = [&](int w) {
     return tile_start(w, W_tiles, NW) != tile_start(w + 1, W_tiles, NW);
   };
-#pragma unroll 1
-  for (int j = 0; j < G; ++j) {
-    float M = -INFINITY;
-    for (int w = w0 + lane; w <= w1; w += 32)
-      if (live(w)) M = fmaxf(M, __ldcg(p.ws_ml + (static_cast<size_t>(slot_of(w)) * G + j) * 2));
+  const float* ml = p.ws_ml;
+  // pass 1: M[j] over all pieces
+  float M[HP];
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, m));
-    float acc[PER];
+  for (int j = 0; j < HP; ++j) M[j] = -INFINITY;
+  for (int w = w0 + lane; w <= w1; w += 32) {
+    if (!live(w)) continue;
+    const float2* mlw =
+        reinterpret_cast<const float2*>(ml) + static_cast<size_t>(slot_of(w)) * G + j0;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float Lsum = 0.f;
-    for (int base = w0; base <= w1; base += 32) {
-      const int w = base + lane;
-      float f = 0.f;
-      if (w <= w1 && live(w)) {
-        const size_t k = (static_cast<size_t>(slot_of(w)) * G + j) * 2;
-        f = ex2(__ldcg(p.ws_ml + k) - M);
-        Lsum += __ldcg(p.ws_ml + k + 1) * f;
-      }
-      const int n = min(32, w1 - base + 1);
-      for (int i = 0; i < n; i += 4) {
-        float fi[4], v[4][PER];
+    for (int j = 0; j < HP; ++j) M[j] = fmaxf(M[j], __ldcg(mlw + j).x);
+  }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          fi[u] = __shfl_sync(kFullMask, f, (i + u) & 31);
+  for (int j = 0; j < HP; ++j)
 #pragma unroll
-          for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
-          if (i + u < n && fi[u] != 0.f) {
-            const float* row =
-                p.ws_o + (static_cast<size_t>(slot_of(base + i + u)) * G + j) * D;
+    for (int m = 16; m >= 1; m >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(kFullMask, M[j], m));
+
+  // pass 2: weights, L[j], and the weighted o rows
+  float acc[HP][PER], Lsum[HP];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) v[u][e] = __ldcg(row + lane + 32 * e);
-          }
-        }
+  for (int j = 0; j < HP; ++j) {
+    Lsum[j] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+    for (int e = 0; e < PER; ++e) acc[j][e] = 0.f;
+  }
+  for (int base = w0; base <= w1; base += 32) {
+    const int w = base + lane;
+    float f[HP];
 #pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] = fmaf(v[u][e], fi[u], acc[e]);
+    for (int j = 0; j < HP; ++j) f[j] = 0.f;
+    if (w <= w1 && live(w)) {
+      const float2* mlw =
+          reinterpret_cast<const float2*>(ml) + static_cast<size_t>(slot_of(w)) * G + j0;
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const float2 v = __ldcg(mlw + j);
+        f[j] = ex2(v.x - M[j]);
+        Lsum[j] += v.y * f[j];
       }
     }
+    const int n = min(32, w1 - base + 1);
+    for (int i = 0; i < n; ++i) {
+      if (!live(base + i)) continue;
+      const float* row = p.ws_o + (static_cast<size_t>(slot_of(base + i)) * G + j0) * D;
+      float v[HP][PER];
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) Lsum += __shfl_xor_sync(kFullMask, Lsum, m);
-    const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j) * D;
+      for (int j = 0; j < HP; ++j)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[j][e] = __ldcg(row + j * D + lane + 32 * e);
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const float fi = __shfl_sync(kFullMask, f[j], i);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[j][e] = fmaf(v[j][e], fi, acc[j][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < HP; ++j) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) Lsum[j] += __shfl_xor_sync(kFullMask, Lsum[j], m);
+    const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j0 + j) * D;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      const float v = acc[e] / Lsum;
+      const float v = acc[j][e] / Lsum[j];
       if (p.out_bf16)
         reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
       else
         reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
     }
   }
+}
+
+// Merges all G heads of a segment, at most four heads per pass (register budget).
+template <int D, int G>
+__device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1, bool w0_tail,
+                              int W_tiles, int NW, int lane) {
+  constexpr int HP = G < 4 ? G : 4;
+#pragma unroll 1
+  for (int j0 = 0; j0 < G; j0 += HP)
+    merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, W_tiles, NW, lane);
 }
 
 template <typename KV, int D, int G>
