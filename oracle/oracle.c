@@ -19,7 +19,8 @@
  *    physical blocks; attention only reads them.
  *  - Request-level transfer of the KV (page on goodput and PD disaggregation,
  *    0539edu.com, sec. 5.4 "request-level granularity"): after prefill the whole KV of
- *    a request is sent in one piece, which needs it gathered into one buffer.
+ *    a request is sent in one piece, which needs it gathered into one buffer (pack) and,
+ *    on the receiving instance, scattered into the blocks allocated there (unpack).
  *
  * Attention is the plain definition, with no online or split softmax:
  *      s_t = scale * sum_d q[d] * K_t[d]            for t < L
@@ -124,6 +125,35 @@ int oracle_kv_pack_blocks(void* out, const void* k_cache, const void* v_cache,
     memcpy(dst + row_bytes, (const char*)v_cache + src, row_bytes);
   }
   return ORC_OK;
+}
+
+/*
+ * KV unpack, the receiving side of a request-level transfer: for t < context_len, write
+ * in[t, 0, h, :] to the K row and in[t, 1, h, :] to the V row of logical token t, token t
+ * being row t % block_size of physical block block_table_row[t / block_size]. Bitwise.
+ * A block id out of range is an error; that token is skipped.
+ */
+int oracle_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
+                            const int32_t* block_table_row, int context_len, int H_kv, int D,
+                            int block_size, int num_blocks, int dtype) {
+  if (context_len < 0 || H_kv <= 0 || D <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      !orc_dtype_ok(dtype))
+    return ORC_ERR_ARG;
+  const size_t e = orc_elem_size(dtype);
+  const size_t row_bytes = (size_t)H_kv * (size_t)D * e;
+  int status = ORC_OK;
+  for (int t = 0; t < context_len; ++t) {
+    const int32_t block = block_table_row[t / block_size];
+    if (block < 0 || block >= num_blocks) {
+      status = ORC_ERR_DATA;
+      continue;
+    }
+    const size_t dst = ((size_t)block * (size_t)block_size + (size_t)(t % block_size)) * row_bytes;
+    const char* src = (const char*)in + (size_t)t * 2u * row_bytes;
+    memcpy((char*)k_cache + dst, src, row_bytes);
+    memcpy((char*)v_cache + dst, src + row_bytes, row_bytes);
+  }
+  return status;
 }
 
 /*

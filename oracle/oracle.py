@@ -53,6 +53,8 @@ def load(path: str | None = None):
         lib.oracle_kv_append.restype = I
         lib.oracle_kv_pack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I]
         lib.oracle_kv_pack_blocks.restype = I
+        lib.oracle_kv_unpack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_kv_unpack_blocks.restype = I
         lib.oracle_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F,
                                                       I, I, I]
         lib.oracle_paged_decode_attention.restype = I
@@ -98,6 +100,17 @@ def kv_pack_blocks(k_cache, v_cache, block_table_row, context_len: int, lib=None
     st = lib.oracle_kv_pack_blocks(_ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(row),
                                    int(context_len), H_kv, D, bs, NB, _dtype_code(k_cache))
     return out, st
+
+
+def kv_unpack_blocks(packed, k_cache, v_cache, block_table_row, context_len: int, lib=None) -> int:
+    """In-place scatter of a dense ``[L, 2, H_kv, D]`` buffer into the caches; returns status."""
+    lib = lib or load()
+    NB, bs, H_kv, D = k_cache.shape
+    assert packed.dtype == k_cache.dtype and packed.shape[1:] == (2, H_kv, D)
+    row = np.ascontiguousarray(block_table_row, dtype=np.int32)
+    return lib.oracle_kv_unpack_blocks(_ptr(np.ascontiguousarray(packed)), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(row), int(context_len), H_kv, D, bs,
+                                       NB, _dtype_code(k_cache))
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,

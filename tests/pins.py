@@ -18,7 +18,9 @@ Facts used:
   - GQA equals MHA with each kv-head replicated;
   - the log-sum-exp merge of pieces equals the whole;
   - output is linear in V;
-  - append then pack gives back the history plus the new token, bit for bit.
+  - append then pack gives back the history plus the new token, bit for bit;
+  - unpack into freshly scattered blocks then pack gives back the buffer, bit for bit, and
+    unpack touches no row outside the request's tokens.
 """
 from __future__ import annotations
 
@@ -282,6 +284,35 @@ def pin_append_then_pack_roundtrip(lib):
                              np.concatenate([p.V[b][:L], new_v[b:b + 1]])], axis=1)
             assert packed.dtype == want.dtype
             assert np.array_equal(packed.view(np.uint8), want.view(np.uint8)), (dtype, b)
+
+
+def pin_unpack_then_pack_roundtrip(lib):
+    rng = np.random.default_rng(22)
+    for dtype in ("f32", "bf16"):
+        H_kv, D, bs = 2, 8, 4
+        for L in (1, 4, 9, 13):
+            NB = (L + bs - 1) // bs + 5
+            table = rng.permutation(NB)[:(L + bs - 1) // bs].astype(np.int32)
+            packed = as_stored(rng.standard_normal((L, 2, H_kv, D)), dtype)
+            kc = as_stored(rng.standard_normal((NB, bs, H_kv, D)), dtype)
+            vc = as_stored(rng.standard_normal((NB, bs, H_kv, D)), dtype)
+            kc0, vc0 = kc.copy(), vc.copy()
+            assert orc.kv_unpack_blocks(packed, kc, vc, table, L, lib=lib) == orc.ORC_OK
+            back, st = orc.kv_pack_blocks(kc, vc, table, L, lib=lib)
+            assert st == orc.ORC_OK
+            assert np.array_equal(back.view(np.uint8), packed.view(np.uint8)), (dtype, L)
+            # rows that hold none of the request's tokens are untouched
+            touched = np.zeros((NB, bs), bool)
+            for t in range(L):
+                touched[table[t // bs], t % bs] = True
+            assert np.array_equal(kc[~touched].view(np.uint8), kc0[~touched].view(np.uint8))
+            assert np.array_equal(vc[~touched].view(np.uint8), vc0[~touched].view(np.uint8))
+            # and the rows it wrote are the buffer's, K and V in their places
+            t = L - 1
+            assert np.array_equal(kc[table[t // bs], t % bs].view(np.uint8),
+                                  packed[t, 0].view(np.uint8))
+            assert np.array_equal(vc[table[t // bs], t % bs].view(np.uint8),
+                                  packed[t, 1].view(np.uint8))
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -46,6 +46,14 @@ MUTANTS = [
       ("memcpy(dst + row_bytes, (const char*)v_cache + src, row_bytes);",
        "memcpy(dst + row_bytes, (const char*)k_cache + src, row_bytes);", None)]),
     ("bf16_upcast_shift", [("((uint32_t)h) << 16", "((uint32_t)h) << 15", None)]),
+    ("unpack_swaps_k_and_v",
+     [("    memcpy((char*)k_cache + dst, src, row_bytes);\n    memcpy((char*)v_cache + dst, src + row_bytes, row_bytes);",
+       "    memcpy((char*)k_cache + dst, src + row_bytes, row_bytes);\n    memcpy((char*)v_cache + dst, src, row_bytes);",
+       None)]),
+    ("unpack_wrong_row",
+     [("((size_t)block * (size_t)block_size + (size_t)(t % block_size)) * row_bytes;\n    const char* src",
+       "((size_t)block * (size_t)block_size + (size_t)((t + 1) % block_size)) * row_bytes;\n    const char* src",
+       None)]),
     ("combine_forgets_weights", [("Lsum += l[j] * exp(m[j] - M);", "Lsum += l[j];", None)]),
 ]
 
