@@ -461,10 +461,69 @@ def sweep_workloads(args, dev, flush, peak):
                           "frac_of_peak": round(gbs / peak, 4),
                           "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
         res_w["bytes"] = nb["attention"]
+        if w.sm_caps_pct:
+            res_w["two_streams"] = overlap_legs(args, s, nb["attention"], sms, flush, peak,
+                                                res_w["all_sms"]["us"])
         out_all[name] = res_w
         del s
         torch.cuda.empty_cache()
     return out_all
+
+
+def overlap_legs(args, s, attn_bytes, sms, flush, peak, t_single_us):
+    """Local + offloaded attention sharing one GPU: the batch is split into a remote part
+    (the first `ratio` of the requests) and a local part, run as two concurrent launches on
+    two streams whose SM caps split the GPU in the same ratio. Reports the time of both
+    together against one launch of the whole batch on every SM."""
+    import torch
+
+    import paged_decode_attention_02_gb300 as pda
+
+    w = s.w
+    dev = s.q.device
+    main = torch.cuda.current_stream(dev)
+    res = {}
+    for ratio in (0.3, 0.5, 0.7):
+        n_r = int(math.ceil(ratio * s.B))
+        cap_r = max(1, int(round(ratio * sms)))
+        parts = [(slice(0, n_r), cap_r), (slice(n_r, s.B), max(1, sms - cap_r))]
+        legs = []
+        for sl, cap in parts:
+            q = s.q[sl].contiguous()
+            legs.append(dict(q=q, bt=s.block_tables[sl].contiguous(),
+                             cl=s.context_lens[sl].contiguous(), out=torch.empty_like(q),
+                             cap=cap, stream=torch.cuda.Stream(dev),
+                             ws=pda.alloc_workspace(q.shape[0], w.H, w.H_kv, w.D, w.block_size,
+                                                    w.torch_dtype, cap, dev)))
+
+        def run():
+            for g in legs:
+                g["stream"].wait_stream(main)
+                pda.paged_decode_attention(g["out"], g["q"], s.k_cache, s.v_cache, g["bt"],
+                                           g["cl"], s.max_context_len, s.scale, sm_cap=g["cap"],
+                                           workspace=g["ws"], stream=g["stream"])
+            for g in legs:
+                main.wait_stream(g["stream"])
+
+        for _ in range(3):
+            flush()
+            run()
+        ts = []
+        for _ in range(args.sweep_iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush()
+            a.record(main)
+            run()
+            b.record(main)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        t = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e-3
+        gbs = attn_bytes / t / 1e9
+        res[f"remote_{int(ratio * 100)}pct"] = {
+            "remote_requests": n_r, "remote_sms": cap_r, "local_sms": sms - cap_r,
+            "us": round(t * 1e6, 2), "GBps": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "vs_one_launch": round(t_single_us / (t * 1e6), 4)}
+    return res
 
 
 # ------------------------------------------------------------------ reference arm

@@ -63,7 +63,7 @@ typedef enum { PDA_F32 = 0, PDA_BF16 = 1 } pda_dtype;
 /* Bytes of the fixed device scratch behind pda_paged_decode_attention_noalloc. */
 #define PDA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
-/* Most requests one batched pack call takes. */
+/* Most requests one batched pack or unpack call takes. */
 #define PDA_PACK_MAX_BATCH 64
 
 /* Human-readable name of a status. Never NULL. */
@@ -224,6 +224,42 @@ pda_status pda_kv_pack_blocks_batched(void* const* outs, const int32_t* const* b
                                       const void* v_cache, int H_kv, int D, int block_size,
                                       int num_blocks, pda_dtype kv_dtype, int32_t* error_word,
                                       cudaStream_t stream);
+
+/*
+ * pda_kv_unpack_blocks -- the receiving side of a request-level KV transfer: scatter one
+ * request's contiguous KV buffer into the blocks allocated for it.
+ *
+ * Defined by the KV migration of PD disaggregation (page on goodput and PD disaggregation,
+ * 0539edu.com, sec. 3: after prefill the request's KV moves to a decode worker; sec. 5.4:
+ * request-level transfer sends it in one piece) into the paged layout, whose blocks are
+ * allocated on demand (page "From PagedAttention to Prefill-Decode disaggregation", sec. 2.2
+ * step 3). The inverse of pda_kv_pack_blocks: for t < context_len, the K row of token t
+ * (row t % block_size of block block_table_row[t / block_size]) = in[t, 0, :, :] and the V
+ * row = in[t, 1, :, :].
+ *
+ *  in             [context_len, 2, H_kv, D] in kv_dtype, dense; read only.
+ *  k_cache,v_cache [num_blocks, block_size, H_kv, D], updated in place; rows of other
+ *                 tokens are not touched.
+ *  A block id out of range sets PDA_DEVERR_BLOCK_ID and that token is not written. Tokens
+ *  that map to the same row race (the caller must not do that). Bitwise copy; 16-byte rows
+ *  and alignment as for pack.
+ */
+pda_status pda_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
+                                const int32_t* block_table_row, int context_len, int H_kv,
+                                int D, int block_size, int num_blocks, pda_dtype kv_dtype,
+                                int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_unpack_blocks_batched -- pda_kv_unpack_blocks for n requests in one launch.
+ *  ins, block_table_rows, context_lens: HOST arrays of n entries (device pointers and host
+ *  counts), copied into the launch. n <= PDA_PACK_MAX_BATCH.
+ */
+pda_status pda_kv_unpack_blocks_batched(const void* const* ins,
+                                        const int32_t* const* block_table_rows,
+                                        const int32_t* context_lens, int n, void* k_cache,
+                                        void* v_cache, int H_kv, int D, int block_size,
+                                        int num_blocks, pda_dtype kv_dtype, int32_t* error_word,
+                                        cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,7 @@ EXPORTED = [
     "pda_status_string", "pda_version", "pda_device_sm_count", "pda_kv_append",
     "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
     "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
+    "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched",
 ]
 
 _lock = threading.Lock()
@@ -72,6 +73,10 @@ def load():
         lib.pda_kv_pack_blocks.restype = I
         lib.pda_kv_pack_blocks_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P, P]
         lib.pda_kv_pack_blocks_batched.restype = I
+        lib.pda_kv_unpack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
+        lib.pda_kv_unpack_blocks.restype = I
+        lib.pda_kv_unpack_blocks_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P, P]
+        lib.pda_kv_unpack_blocks_batched.restype = I
         _lib = lib
         return lib
 
@@ -206,3 +211,29 @@ def kv_pack_blocks_batched(outs, k_cache, v_cache, block_table_rows, context_len
                                              _ptr(error_word), _stream(stream)),
            "pda_kv_pack_blocks_batched")
     return outs
+
+
+def kv_unpack_blocks(packed, k_cache, v_cache, block_table_row, context_len: int,
+                     error_word=None, stream=None):
+    """Scatter one request's ``[context_len, 2, H_kv, D]`` buffer into its cache blocks."""
+    NB, bs, H_kv, D = k_cache.shape
+    assert packed.shape[0] >= context_len and tuple(packed.shape[1:]) == (2, H_kv, D)
+    _check(load().pda_kv_unpack_blocks(_ptr(packed), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_table_row), int(context_len), H_kv, D, bs,
+                                       NB, _dtype(k_cache), _ptr(error_word), _stream(stream)),
+           "pda_kv_unpack_blocks")
+
+
+def kv_unpack_blocks_batched(packed, k_cache, v_cache, block_table_rows, context_lens,
+                             error_word=None, stream=None):
+    """``kv_unpack_blocks`` for several requests in one launch."""
+    NB, bs, H_kv, D = k_cache.shape
+    n = len(packed)
+    assert len(block_table_rows) == n and len(context_lens) == n
+    in_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(x).value for x in packed])
+    row_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(r).value for r in block_table_rows])
+    len_arr = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in context_lens])
+    _check(load().pda_kv_unpack_blocks_batched(in_arr, row_arr, len_arr, n, _ptr(k_cache),
+                                               _ptr(v_cache), H_kv, D, bs, NB, _dtype(k_cache),
+                                               _ptr(error_word), _stream(stream)),
+           "pda_kv_unpack_blocks_batched")

@@ -1,7 +1,8 @@
-// kv_ops.cu -- KV append (scatter of each request's new token into its slot) and KV pack
-// (gather of one request's scattered blocks into a contiguous transfer buffer), sm_103a.
+// kv_ops.cu -- KV append (scatter of each request's new token into its slot), KV pack
+// (gather of one request's scattered blocks into a contiguous transfer buffer) and KV
+// unpack (the receiving side: scatter of such a buffer into freshly allocated blocks).
 //
-// Both are pure copies of rows of H_kv * D elements, done as 16-byte vectors with
+// All three are pure copies of rows of H_kv * D elements, done as 16-byte vectors with
 // streaming (evict-first) loads and stores so a large pack does not flush L2.
 //  * append: each decode step writes the new token's K/V (page "Disaggregated LLM
 //    Serving: from PD disaggregation to attention offload", sec. 1, second list item 2)
@@ -9,6 +10,9 @@
 //  * pack: request-level KV transfer needs the request's KV in one buffer (page on goodput
 //    and PD disaggregation, 0539edu.com, sec. 5.4); out[t] = (K row, V row) of token t,
 //    token t being row t % block_size of block table[t / block_size].
+//  * unpack: the decode instance receives that buffer and writes it into the blocks it
+//    allocated for the request (same page, sec. 3: the KV is migrated to the decode worker;
+//    page "From PagedAttention to Prefill-Decode disaggregation", sec. 2.2 step 3).
 #include "pda_device.cuh"
 #include "pda_internal.h"
 
@@ -46,14 +50,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
 }
 
 struct PackJob {
-  uint4* out;
+  uint4* buf;  // the request's dense [len, 2, H_kv, D] buffer (pack: written, unpack: read)
   const int32_t* table;
   int len;
 };
 
 struct PackParams {
-  const uint4* k_cache;
-  const uint4* v_cache;
+  uint4* k_cache;
+  uint4* v_cache;
   int32_t* error_word;
   int n, row_vecs, block_size, num_blocks;
   PackJob jobs[PDA_PACK_MAX_BATCH];
@@ -61,9 +65,13 @@ struct PackParams {
 
 constexpr int kPackUnroll = 4;
 
+// Pack (cache rows -> dense buffer) or unpack (dense buffer -> cache rows).
 // blockIdx.y selects the request; the x-dimension strides over its (token, K|V, vector)
 // copies with kPackUnroll independent 16-byte loads in flight per thread.
-__global__ void __launch_bounds__(256) kv_pack_kernel(const __grid_constant__ PackParams p) {
+// Pack: a token in a block out of range reads as 0xFF bytes. Unpack: it is not written.
+// Both set PDA_DEVERR_BLOCK_ID.
+template <bool kUnpack>
+__global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ PackParams p) {
   const PackJob job = p.jobs[blockIdx.y];
   const int rv = p.row_vecs;
   const long long total = static_cast<long long>(job.len) * 2 * rv;
@@ -72,24 +80,30 @@ __global__ void __launch_bounds__(256) kv_pack_kernel(const __grid_constant__ Pa
                         threadIdx.x;
        base < total; base += step) {
     uint4 v[kPackUnroll];
+    size_t row_at[kPackUnroll];  // cache vector index of copy u
     bool bad[kPackUnroll];
+    int which[kPackUnroll];
 #pragma unroll
     for (int u = 0; u < kPackUnroll; ++u) {
       const long long i = base + static_cast<long long>(u) * blockDim.x;
       bad[u] = false;
+      which[u] = 0;
+      row_at[u] = 0;
       if (i < total) {
         const int t = static_cast<int>(i / (2 * rv));
         const int rem = static_cast<int>(i % (2 * rv));
-        const int which = rem / rv;
+        which[u] = rem / rv;
         const int c = rem % rv;
         const int blk = job.table[t / p.block_size];
-        if (blk < 0 || blk >= p.num_blocks) {
-          bad[u] = true;
+        bad[u] = blk < 0 || blk >= p.num_blocks;
+        if (!bad[u])
+          row_at[u] = (static_cast<size_t>(blk) * p.block_size + t % p.block_size) * rv + c;
+        if (kUnpack) {
+          v[u] = __ldcs(job.buf + i);
+        } else if (bad[u]) {
           v[u] = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
         } else {
-          const size_t src =
-              (static_cast<size_t>(blk) * p.block_size + t % p.block_size) * rv + c;
-          v[u] = __ldcs(which == 0 ? p.k_cache + src : p.v_cache + src);
+          v[u] = __ldcs((which[u] == 0 ? p.k_cache : p.v_cache) + row_at[u]);
         }
       }
     }
@@ -98,7 +112,10 @@ __global__ void __launch_bounds__(256) kv_pack_kernel(const __grid_constant__ Pa
       const long long i = base + static_cast<long long>(u) * blockDim.x;
       if (i < total) {
         if (bad[u] && (i % (2 * rv)) == 0) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
-        __stcs(job.out + i, v[u]);
+        if (!kUnpack)
+          __stcs(job.buf + i, v[u]);
+        else if (!bad[u])
+          __stcs((which[u] == 0 ? p.k_cache : p.v_cache) + row_at[u], v[u]);
       }
     }
   }
@@ -117,13 +134,60 @@ pda_status check_kv_rows(int H_kv, int D, int block_size, int num_blocks, pda_dt
   return PDA_OK;
 }
 
-pda_status launch_pack(const PackParams& p, long long max_total, cudaStream_t stream) {
+pda_status launch_blocks(const PackParams& p, long long max_total, bool unpack,
+                         cudaStream_t stream) {
   const long long per_block = 256ll * kPackUnroll;
   long long gx = (max_total + per_block - 1) / per_block;
   if (gx > 4096) gx = 4096;
   if (gx < 1) gx = 1;
-  kv_pack_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.n)), 256, 0, stream>>>(p);
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.n));
+  if (unpack)
+    kv_blocks_kernel<true><<<grid, 256, 0, stream>>>(p);
+  else
+    kv_blocks_kernel<false><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
+// Shared front end of the batched pack and unpack calls: validates, fills the jobs, launches.
+pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_rows,
+                          const int32_t* context_lens, int n, const void* k_cache,
+                          const void* v_cache, int H_kv, int D, int block_size, int num_blocks,
+                          pda_dtype kv_dtype, int32_t* error_word, bool unpack,
+                          cudaStream_t stream) {
+  if (n < 0 || n > PDA_PACK_MAX_BATCH) return n < 0 ? PDA_ERR_INVALID_ARG : PDA_ERR_UNSUPPORTED;
+  int rv = 0;
+  const pda_status st = check_kv_rows(H_kv, D, block_size, num_blocks, kv_dtype, &rv);
+  if (st != PDA_OK) return st;
+  if (n == 0) return PDA_OK;
+  if (bufs == nullptr || block_table_rows == nullptr || context_lens == nullptr ||
+      k_cache == nullptr || v_cache == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PDA_ERR_INVALID_ARG;
+  PackParams p;
+  p.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+  p.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+  p.error_word = error_word;
+  p.row_vecs = rv;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  int m = 0;
+  long long max_total = 0;
+  for (int i = 0; i < n; ++i) {
+    const int len = context_lens[i];
+    if (len < 0) return PDA_ERR_INVALID_ARG;
+    if (len == 0) continue;
+    if (bufs[i] == nullptr || block_table_rows[i] == nullptr || !aligned16(bufs[i]))
+      return PDA_ERR_INVALID_ARG;
+    p.jobs[m].buf = static_cast<uint4*>(bufs[i]);
+    p.jobs[m].table = block_table_rows[i];
+    p.jobs[m].len = len;
+    const long long tot = static_cast<long long>(len) * 2 * rv;
+    if (tot > max_total) max_total = tot;
+    ++m;
+  }
+  if (m == 0) return PDA_OK;
+  p.n = m;
+  return launch_blocks(p, max_total, unpack, stream);
 }
 
 }  // namespace
@@ -162,40 +226,8 @@ extern "C" pda_status pda_kv_pack_blocks_batched(void* const* outs,
                                                  int H_kv, int D, int block_size, int num_blocks,
                                                  pda_dtype kv_dtype, int32_t* error_word,
                                                  cudaStream_t stream) {
-  if (n < 0 || n > PDA_PACK_MAX_BATCH) return n < 0 ? PDA_ERR_INVALID_ARG : PDA_ERR_UNSUPPORTED;
-  int rv = 0;
-  const pda_status st = check_kv_rows(H_kv, D, block_size, num_blocks, kv_dtype, &rv);
-  if (st != PDA_OK) return st;
-  if (n == 0) return PDA_OK;
-  if (outs == nullptr || block_table_rows == nullptr || context_lens == nullptr ||
-      k_cache == nullptr || v_cache == nullptr)
-    return PDA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return PDA_ERR_INVALID_ARG;
-  PackParams p;
-  p.k_cache = static_cast<const uint4*>(k_cache);
-  p.v_cache = static_cast<const uint4*>(v_cache);
-  p.error_word = error_word;
-  p.row_vecs = rv;
-  p.block_size = block_size;
-  p.num_blocks = num_blocks;
-  int m = 0;
-  long long max_total = 0;
-  for (int i = 0; i < n; ++i) {
-    const int len = context_lens[i];
-    if (len < 0) return PDA_ERR_INVALID_ARG;
-    if (len == 0) continue;
-    if (outs[i] == nullptr || block_table_rows[i] == nullptr || !aligned16(outs[i]))
-      return PDA_ERR_INVALID_ARG;
-    p.jobs[m].out = static_cast<uint4*>(outs[i]);
-    p.jobs[m].table = block_table_rows[i];
-    p.jobs[m].len = len;
-    const long long tot = static_cast<long long>(len) * 2 * rv;
-    if (tot > max_total) max_total = tot;
-    ++m;
-  }
-  if (m == 0) return PDA_OK;
-  p.n = m;
-  return launch_pack(p, max_total, stream);
+  return blocks_batched(outs, block_table_rows, context_lens, n, k_cache, v_cache, H_kv, D,
+                        block_size, num_blocks, kv_dtype, error_word, false, stream);
 }
 
 extern "C" pda_status pda_kv_pack_blocks(void* out, const void* k_cache, const void* v_cache,
@@ -208,4 +240,28 @@ extern "C" pda_status pda_kv_pack_blocks(void* out, const void* k_cache, const v
   const int32_t lens[1] = {context_len};
   return pda_kv_pack_blocks_batched(outs, rows, lens, 1, k_cache, v_cache, H_kv, D, block_size,
                                     num_blocks, kv_dtype, error_word, stream);
+}
+
+extern "C" pda_status pda_kv_unpack_blocks_batched(const void* const* ins,
+                                                   const int32_t* const* block_table_rows,
+                                                   const int32_t* context_lens, int n,
+                                                   void* k_cache, void* v_cache, int H_kv, int D,
+                                                   int block_size, int num_blocks,
+                                                   pda_dtype kv_dtype, int32_t* error_word,
+                                                   cudaStream_t stream) {
+  return blocks_batched(const_cast<void* const*>(ins), block_table_rows, context_lens, n,
+                        k_cache, v_cache, H_kv, D, block_size, num_blocks, kv_dtype, error_word,
+                        true, stream);
+}
+
+extern "C" pda_status pda_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
+                                           const int32_t* block_table_row, int context_len,
+                                           int H_kv, int D, int block_size, int num_blocks,
+                                           pda_dtype kv_dtype, int32_t* error_word,
+                                           cudaStream_t stream) {
+  const void* ins[1] = {in};
+  const int32_t* rows[1] = {block_table_row};
+  const int32_t lens[1] = {context_len};
+  return pda_kv_unpack_blocks_batched(ins, rows, lens, 1, k_cache, v_cache, H_kv, D,
+                                      block_size, num_blocks, kv_dtype, error_word, stream);
 }

@@ -313,3 +313,104 @@ def test_workspace_too_small_is_rejected():
         pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
                                    s.context_lens, s.max_context_len, s.scale, workspace=ws)
     assert e.value.status == binding.PDA_ERR_WORKSPACE
+
+
+# ------------------------------------------------------------------ two concurrent launches
+@pytest.mark.parametrize("ratio", [0.3, 0.5])
+def test_local_and_remote_attention_on_two_streams(ratio):
+    """The batch split into a 'remote' and a 'local' part, run as two attention launches on
+    two streams at once with complementary SM caps (attention offload sharing one GPU)."""
+    s = wl.make_step("sm_sweep_b128", device=DEV, B=24)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0
+    sms = pda.device_sm_count()
+    n_r = int(np.ceil(ratio * s.B))
+    cap_r = max(1, int(round(ratio * sms)))
+    cap_l = max(1, sms - cap_r)
+    parts = [(slice(0, n_r), cap_r), (slice(n_r, s.B), cap_l)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs, errs, keep = [], [], []
+    main = torch.cuda.current_stream()
+    for (sl, cap), stream in zip(parts, streams):
+        q = s.q[sl].contiguous()
+        bt = s.block_tables[sl].contiguous()
+        cl = s.context_lens[sl].contiguous()
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ws = pda.alloc_workspace(q.shape[0], s.w.H, s.w.H_kv, s.w.D, 16, q.dtype, cap, DEV)
+        keep += [q, bt, cl, ws]
+        stream.wait_stream(main)
+        with torch.cuda.stream(stream):
+            pda.paged_decode_attention(out, q, s.k_cache, s.v_cache, bt, cl,
+                                       s.max_context_len, s.scale, sm_cap=cap, workspace=ws,
+                                       error_word=err, stream=stream)
+        outs.append(out)
+        errs.append(err)
+    for stream in streams:
+        main.wait_stream(stream)
+    torch.cuda.synchronize()
+    assert all(int(e.item()) == 0 for e in errs)
+    assert_attention_close(torch.cat(outs), ref, f"two streams, ratio {ratio}", strict=True)
+
+
+# ------------------------------------------------------------------ KV unpack
+@pytest.mark.parametrize("name,B", [("tiny", None), ("llama2_13b_b80", 6)])
+def test_unpack_matches_oracle_bit_for_bit(name, B):
+    s = wl.make_step(name, device=DEV, B=B)
+    w = s.w
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(77)
+    kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
+    bufs, rows, lens = [], [], []
+    for b in range(s.B):
+        L = int(s.context_lens_np[b])
+        buf = torch.randn((L, 2, w.H_kv, w.D), generator=gen, device=DEV).to(w.torch_dtype)
+        bufs.append(buf)
+        rows.append(s.block_tables[b])
+        lens.append(L)
+        assert orc.kv_unpack_blocks(to_np(buf), kc, vc, s.block_tables_np[b], L) == 0
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_unpack_blocks(bufs[0], s.k_cache, s.v_cache, rows[0], lens[0], error_word=err)
+    pda.kv_unpack_blocks_batched(bufs[1:], s.k_cache, s.v_cache, rows[1:], lens[1:],
+                                 error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
+
+
+def test_full_size_unpack_then_pack_of_longest_requests():
+    s = wl.make_step("gqa_skew_b256", device=DEV)
+    w = s.w
+    reqs = s.pack_requests
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(78)
+    ins = [torch.randn((int(s.context_lens_np[r]), 2, w.H_kv, w.D), generator=gen,
+                       device=DEV).to(w.torch_dtype) for r in reqs]
+    rows = [s.block_tables[r] for r in reqs]
+    lens = [int(s.context_lens_np[r]) for r in reqs]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_unpack_blocks_batched(ins, s.k_cache, s.v_cache, rows, lens, error_word=err)
+    outs = [torch.empty_like(x) for x in ins]
+    pda.kv_pack_blocks_batched(outs, s.k_cache, s.v_cache, rows, lens, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for a, b in zip(ins, outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_unpack_bad_block_is_skipped_with_error_bit():
+    s = wl.make_step("tiny", device=DEV)
+    b = 3
+    L = int(s.context_lens_np[b])
+    s.block_tables[b, 1] = s.num_blocks + 2
+    buf = torch.full((L, 2, s.w.H_kv, s.w.D), 7.0, dtype=s.k_cache.dtype, device=DEV)
+    before = s.k_cache.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_unpack_blocks(buf, s.k_cache, s.v_cache, s.block_tables[b], L, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == binding.PDA_DEVERR_BLOCK_ID
+    kc = to_np(before).copy()
+    vc = to_np(s.v_cache).copy()
+    bt = s.block_tables[b].cpu().numpy()
+    orc.kv_unpack_blocks(to_np(buf), kc, vc, bt, L)  # the oracle skips the same tokens
+    assert np.array_equal(to_np(s.k_cache), kc)
