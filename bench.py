@@ -355,6 +355,22 @@ def run_ours(args, ws, rank, local):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during timing")
 
+    # ---- unpack (the receiving side of the transfer): write the packed buffers back into
+    # their own blocks, which leaves the cache unchanged
+    t_unpack = None
+    if pack_reqs:
+        uev = []
+        for _ in range(args.warmup + args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush()
+            a.record(stream)
+            pda.kv_unpack_blocks_batched(packs, s.k_cache, s.v_cache, pack_rows, pack_lens,
+                                         error_word=err)
+            b.record(stream)
+            uev.append((a, b))
+        torch.cuda.synchronize()
+        t_unpack = float(np.mean([a.elapsed_time(b) for a, b in uev[args.warmup:]])) * 1e-3
+
     peak, peak_src = hbm_peak()
     attn_gbs = nb["attention"] / t_attn / 1e9
     traffic = profiled_traffic(w.name) if (args.batch is None and cap == 0) else None
@@ -387,6 +403,8 @@ def run_ours(args, ws, rank, local):
         "pack": {"us": round(t_pack * 1e6, 2),
                  "GBps": round(nb["pack"] / t_pack / 1e9, 1) if t_pack > 0 else None,
                  "bytes": nb["pack"]},
+        "unpack": ({"us": round(t_unpack * 1e6, 2), "GBps": round(nb["pack"] / t_unpack / 1e9, 1),
+                    "bytes": nb["pack"], "note": "not part of the step"} if t_unpack else None),
         "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
                      "traffic": traffic, "kernel": "paged_decode_attention call "

@@ -63,59 +63,60 @@ struct PackParams {
   PackJob jobs[PDA_PACK_MAX_BATCH];
 };
 
-constexpr int kPackUnroll = 4;
+constexpr int kPackTokens = 4;  // tokens per thread per iteration (loads in flight)
 
 // Pack (cache rows -> dense buffer) or unpack (dense buffer -> cache rows).
-// blockIdx.y selects the request; the x-dimension strides over its (token, K|V, vector)
-// copies with kPackUnroll independent 16-byte loads in flight per thread.
+// blockIdx.y selects the request. A token's copy is its K row then its V row, 2 * row_vecs
+// 16-byte vectors; thread i of the block always moves vectors i, i + blockDim.x, ... of a
+// token (so no per-vector division), for kPackTokens tokens at a time.
 // Pack: a token in a block out of range reads as 0xFF bytes. Unpack: it is not written.
 // Both set PDA_DEVERR_BLOCK_ID.
 template <bool kUnpack>
 __global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ PackParams p) {
   const PackJob job = p.jobs[blockIdx.y];
   const int rv = p.row_vecs;
-  const long long total = static_cast<long long>(job.len) * 2 * rv;
-  const long long step = static_cast<long long>(gridDim.x) * blockDim.x * kPackUnroll;
-  for (long long base = blockIdx.x * static_cast<long long>(blockDim.x) * kPackUnroll +
-                        threadIdx.x;
-       base < total; base += step) {
-    uint4 v[kPackUnroll];
-    size_t row_at[kPackUnroll];  // cache vector index of copy u
-    bool bad[kPackUnroll];
-    int which[kPackUnroll];
+  const int row2 = 2 * rv;
+  const int bs = p.block_size;
+  for (int t0 = blockIdx.x * kPackTokens; t0 < job.len; t0 += gridDim.x * kPackTokens) {
+    int blk[kPackTokens];
 #pragma unroll
-    for (int u = 0; u < kPackUnroll; ++u) {
-      const long long i = base + static_cast<long long>(u) * blockDim.x;
-      bad[u] = false;
-      which[u] = 0;
-      row_at[u] = 0;
-      if (i < total) {
-        const int t = static_cast<int>(i / (2 * rv));
-        const int rem = static_cast<int>(i % (2 * rv));
-        which[u] = rem / rv;
-        const int c = rem % rv;
-        const int blk = job.table[t / p.block_size];
-        bad[u] = blk < 0 || blk >= p.num_blocks;
-        if (!bad[u])
-          row_at[u] = (static_cast<size_t>(blk) * p.block_size + t % p.block_size) * rv + c;
-        if (kUnpack) {
-          v[u] = __ldcs(job.buf + i);
-        } else if (bad[u]) {
-          v[u] = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
-        } else {
-          v[u] = __ldcs((which[u] == 0 ? p.k_cache : p.v_cache) + row_at[u]);
-        }
+    for (int k = 0; k < kPackTokens; ++k) {
+      const int t = t0 + k;
+      blk[k] = t < job.len ? job.table[t / bs] : 0;
+      if (t < job.len && (blk[k] < 0 || blk[k] >= p.num_blocks)) {
+        if (threadIdx.x == 0) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+        blk[k] = -1;
       }
     }
+    for (int c = threadIdx.x; c < row2; c += blockDim.x) {
+      const bool is_v = c >= rv;
+      const int cv = is_v ? c - rv : c;
+      uint4* cache = is_v ? p.v_cache : p.k_cache;
+      uint4 v[kPackTokens];
 #pragma unroll
-    for (int u = 0; u < kPackUnroll; ++u) {
-      const long long i = base + static_cast<long long>(u) * blockDim.x;
-      if (i < total) {
-        if (bad[u] && (i % (2 * rv)) == 0) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+      for (int k = 0; k < kPackTokens; ++k) {
+        const int t = t0 + k;
+        if (t >= job.len) continue;
+        const size_t buf_at = static_cast<size_t>(t) * row2 + c;
+        const size_t row_at =
+            (static_cast<size_t>(blk[k] < 0 ? 0 : blk[k]) * bs + t % bs) * rv + cv;
+        if (kUnpack)
+          v[k] = __ldcs(job.buf + buf_at);
+        else
+          v[k] = blk[k] < 0 ? make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu)
+                            : __ldcs(cache + row_at);
+      }
+#pragma unroll
+      for (int k = 0; k < kPackTokens; ++k) {
+        const int t = t0 + k;
+        if (t >= job.len) continue;
+        const size_t buf_at = static_cast<size_t>(t) * row2 + c;
+        const size_t row_at =
+            (static_cast<size_t>(blk[k] < 0 ? 0 : blk[k]) * bs + t % bs) * rv + cv;
         if (!kUnpack)
-          __stcs(job.buf + i, v[u]);
-        else if (!bad[u])
-          __stcs((which[u] == 0 ? p.k_cache : p.v_cache) + row_at[u], v[u]);
+          __stcs(job.buf + buf_at, v[k]);
+        else if (blk[k] >= 0)
+          __stcs(cache + row_at, v[k]);
       }
     }
   }
@@ -134,17 +135,17 @@ pda_status check_kv_rows(int H_kv, int D, int block_size, int num_blocks, pda_dt
   return PDA_OK;
 }
 
-pda_status launch_blocks(const PackParams& p, long long max_total, bool unpack,
-                         cudaStream_t stream) {
-  const long long per_block = 256ll * kPackUnroll;
-  long long gx = (max_total + per_block - 1) / per_block;
-  if (gx > 4096) gx = 4096;
+pda_status launch_blocks(const PackParams& p, int max_len, bool unpack, cudaStream_t stream) {
+  int gx = (max_len + kPackTokens - 1) / kPackTokens;
+  if (gx > 8192) gx = 8192;
   if (gx < 1) gx = 1;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.n));
+  // one thread per 16-byte vector of a token's K|V row, at most 256
+  const int threads = 2 * p.row_vecs >= 256 ? 256 : (2 * p.row_vecs + 31) / 32 * 32;
   if (unpack)
-    kv_blocks_kernel<true><<<grid, 256, 0, stream>>>(p);
+    kv_blocks_kernel<true><<<grid, threads, 0, stream>>>(p);
   else
-    kv_blocks_kernel<false><<<grid, 256, 0, stream>>>(p);
+    kv_blocks_kernel<false><<<grid, threads, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
 }
 
@@ -171,7 +172,7 @@ pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_r
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   int m = 0;
-  long long max_total = 0;
+  int max_len = 0;
   for (int i = 0; i < n; ++i) {
     const int len = context_lens[i];
     if (len < 0) return PDA_ERR_INVALID_ARG;
@@ -181,13 +182,12 @@ pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_r
     p.jobs[m].buf = static_cast<uint4*>(bufs[i]);
     p.jobs[m].table = block_table_rows[i];
     p.jobs[m].len = len;
-    const long long tot = static_cast<long long>(len) * 2 * rv;
-    if (tot > max_total) max_total = tot;
+    if (len > max_len) max_len = len;
     ++m;
   }
   if (m == 0) return PDA_OK;
   p.n = m;
-  return launch_blocks(p, max_total, unpack, stream);
+  return launch_blocks(p, max_len, unpack, stream);
 }
 
 }  // namespace
