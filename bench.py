@@ -479,6 +479,8 @@ def sweep_workloads(args, dev, flush, peak):
                           "frac_of_peak": round(gbs / peak, 4),
                           "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
         res_w["bytes"] = nb["attention"]
+        if name == "llama2_7b_b8":
+            res_w["host_overhead_per_layer"] = graph_legs(args, s, sms)
         if w.sm_caps_pct:
             res_w["two_streams"] = overlap_legs(args, s, nb["attention"], sms, flush, peak,
                                                 res_w["all_sms"]["us"])
@@ -486,6 +488,64 @@ def sweep_workloads(args, dev, flush, peak):
         del s
         torch.cuda.empty_cache()
     return out_all
+
+
+def graph_legs(args, s, sms):
+    """Host cost of issuing one decode step (append + attention) per layer, eager through
+    the C ABI against a replay of a bucketed CUDA graph, on the Llama-2-7B batch-8 shape of
+    the pages' per-layer example. Host us = wall time to issue the step (no sync inside the
+    loop); GPU us = device time of the step from CUDA events."""
+    import torch
+
+    import paged_decode_attention_02_gb300 as pda
+    from paged_decode_attention_02_gb300 import graphs as pg
+
+    dev = s.q.device
+    main = torch.cuda.current_stream(dev)
+    out = torch.empty_like(s.q)
+    ws = pda.alloc_workspace(s.B, s.w.H, s.w.H_kv, s.w.D, s.w.block_size, s.w.torch_dtype, 0,
+                             dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    n = 200
+
+    def eager():
+        pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                   s.context_lens, s.max_context_len, s.scale, workspace=ws,
+                                   error_word=err)
+
+    def measure(fn):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        host = (time.perf_counter() - t0) / n
+        b.record(main)
+        torch.cuda.synchronize()
+        return {"host_us": round(host * 1e6, 2), "gpu_us": round(a.elapsed_time(b) * 1e3 / n, 2)}
+
+    res = {"eager_per_layer": measure(eager)}
+    g = pg.DecodeStepGraphs(s.k_cache, s.v_cache, s.w.H, s.max_blocks, max_local=s.B,
+                            max_remote=s.B, interval=max(1, s.B // 2), scale=s.scale,
+                            remote_sm_cap=max(1, int(round(0.3 * sms)))).capture()
+    part = {"q": s.q, "k_new": s.k_new, "v_new": s.v_new, "slot_mapping": s.slot_mapping,
+            "block_tables": s.block_tables, "context_lens": s.context_lens}
+    n_r = max(1, int(round(0.3 * s.B)))
+    loc = {k: v[n_r:] for k, v in part.items()}
+    rem = {k: v[:n_r] for k, v in part.items()}
+    for key, (lp, rp) in {"all_local": (part, None),
+                          f"{n_r}_of_{s.B}_offloaded": (loc, rem)}.items():
+        res[f"graph_stage_per_step_{key}"] = measure(lambda: g.stage(lp, rp))
+        bucket = g.stage(lp, rp)
+        res[f"graph_replay_per_layer_{key}"] = measure(lambda: g.replay(bucket))
+    res["note"] = ("the step's inputs are staged once per step; each layer replays a graph. "
+                   "The pages' per-layer figure for this shape (whole layer, A100, vLLM): "
+                   "380 us GPU, 1137 us CPU")
+    return res
 
 
 def overlap_legs(args, s, attn_bytes, sms, flush, peak, t_single_us):

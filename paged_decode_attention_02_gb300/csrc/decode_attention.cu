@@ -34,6 +34,8 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "pda_device.cuh"
 #include "pda_internal.h"
@@ -826,6 +828,58 @@ bool supported_g(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 // Numbers the calls, so a call recognises arrival counters left by earlier ones.
 std::atomic<unsigned long long> g_call{1};
 
+// Raises a kernel's dynamic shared-memory limit to the full budget once per device, so
+// later calls (and calls made while a stream is being captured) skip the runtime call.
+std::mutex g_attr_mu;
+std::vector<std::pair<const void*, int>> g_attr_done;
+
+pda_status allow_max_smem(const void* fn, int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const auto& e : g_attr_done)
+    if (e.first == fn && e.second == dev) return PDA_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) !=
+      cudaSuccess)
+    return PDA_ERR_CUDA;
+  g_attr_done.emplace_back(fn, dev);
+  return PDA_OK;
+}
+
+// The last few encoded KV tensor maps, keyed by everything the encoding depends on.
+struct MapKey {
+  const void* base;
+  int num_blocks, block_size, H_kv, D, dtype;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && num_blocks == o.num_blocks && block_size == o.block_size &&
+           H_kv == o.H_kv && D == o.D && dtype == o.dtype;
+  }
+};
+constexpr int kMapCache = 8;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
+                                int block_size, int H_kv, int D, pda_dtype dtype) {
+  const MapKey key{base, num_blocks, block_size, H_kv, D, static_cast<int>(dtype)};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_key[i] == key) {
+        *tm = g_map_val[i];
+        return PDA_OK;
+      }
+  }
+  const pda_status st = encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype);
+  if (st != PDA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  g_map_key[g_map_next] = key;
+  g_map_val[g_map_next] = *tm;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_used < kMapCache) ++g_map_used;
+  return PDA_OK;
+}
+
 }  // namespace
 }  // namespace pda
 
@@ -884,15 +938,13 @@ extern "C" pda_status pda_paged_decode_attention(
 
   KernelFn fn = pick_kernel(kv_dtype, D, G);
   if (fn == nullptr) return PDA_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
-    return PDA_ERR_CUDA;
+  st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
+  if (st != PDA_OK) return st;
 
   CUtensorMap tmK, tmV;
-  st = encode_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, D, kv_dtype);
   if (st != PDA_OK) return st;
-  st = encode_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, D, kv_dtype);
   if (st != PDA_OK) return st;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
