@@ -26,7 +26,10 @@
  *      s_t = scale * sum_d q[d] * K_t[d]            for t < L
  *      p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
  *      out = sum_t p_t * V_t
- * Everything is computed in double; stored bf16/fp32 inputs are upcast exactly.
+ * Everything is computed in double; stored bf16/fp32 inputs are upcast exactly, and FP8
+ * E4M3 codes are decoded exactly and multiplied by their tensor's scale. Quantised KV
+ * caches (page "From PagedAttention to Prefill-Decode disaggregation", sec. 6.2: a 4-bit KV
+ * cache dequantised to FP8 before attention) are read through that decode.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - Cache tensors are dense row-major [num_blocks, block_size, H_kv, D].
@@ -49,15 +52,34 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8_E4M3 = 2 };
 enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_DATA = 4 };
 
-static size_t orc_elem_size(int dtype) { return dtype == ORC_BF16 ? 2u : 4u; }
+static size_t orc_elem_size(int dtype) {
+  return dtype == ORC_BF16 ? 2u : (dtype == ORC_FP8_E4M3 ? 1u : 4u);
+}
 
-static int orc_dtype_ok(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF16; }
+static int orc_dtype_ok(int dtype) {
+  return dtype == ORC_F32 || dtype == ORC_BF16 || dtype == ORC_FP8_E4M3;
+}
+
+/*
+ * FP8 E4M3 (the OCP 8-bit format with no infinities): sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits. Exponent 0 encodes subnormals m/8 * 2^-6; exponent 15 with mantissa 7
+ * is NaN; every other code is (1 + m/8) * 2^(e - 7). Largest finite magnitude 448.
+ */
+static double orc_e4m3(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+double oracle_decode_e4m3(int code) { return orc_e4m3((uint8_t)(code & 255)); }
 
 /* Exact upcast of stored element idx. A bf16 value is the upper 16 bits of a binary32. */
 static double orc_load(const void* base, size_t idx, int dtype) {
+  if (dtype == ORC_FP8_E4M3) return orc_e4m3(((const uint8_t*)base)[idx]);
   if (dtype == ORC_BF16) {
     uint16_t h;
     memcpy(&h, (const char*)base + idx * 2u, 2u);
@@ -162,15 +184,15 @@ int oracle_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
  */
 static int orc_gather(double* Kc, double* Vc, const void* k_cache, const void* v_cache,
                       const int32_t* table_row, int L, int hk, int H_kv, int D, int block_size,
-                      int num_blocks, int kv_dtype) {
+                      int num_blocks, int kv_dtype, double k_scale, double v_scale) {
   for (int t = 0; t < L; ++t) {
     const int32_t block = table_row[t / block_size];
     if (block < 0 || block >= num_blocks) return -1;
     const size_t row = (size_t)block * (size_t)block_size + (size_t)(t % block_size);
     const size_t base = (row * (size_t)H_kv + (size_t)hk) * (size_t)D;
     for (int d = 0; d < D; ++d) {
-      Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype);
-      Vc[(size_t)t * D + d] = orc_load(v_cache, base + d, kv_dtype);
+      Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype) * k_scale;
+      Vc[(size_t)t * D + d] = orc_load(v_cache, base + d, kv_dtype) * v_scale;
     }
   }
   return 0;
@@ -184,13 +206,16 @@ static void orc_fill_rows(double* out, int b, int H, int D, double value) {
  * Decode attention over the paged cache. out is [B, H, D] doubles. q is [B, H, D] in
  * q_dtype; caches are [num_blocks, block_size, H_kv, D] in kv_dtype; block_tables is
  * [B, max_blocks]; context_lens is [B]. scale is the binary32 value a caller passes to
- * the kernel, used upcast to double. num_threads <= 0 uses the OpenMP default.
+ * the kernel, used upcast to double. A stored K element means its decoded value times
+ * k_scale, a V element its value times v_scale (1 for unquantised caches; for FP8 caches
+ * the per-tensor scales of the quantisation). num_threads <= 0 uses the OpenMP default.
  */
 int oracle_paged_decode_attention(double* out, const void* q, const void* k_cache,
                                   const void* v_cache, const int32_t* block_tables,
                                   int max_blocks, const int32_t* context_lens, int B, int H,
                                   int H_kv, int D, int block_size, int num_blocks, float scale,
-                                  int q_dtype, int kv_dtype, int num_threads) {
+                                  int q_dtype, int kv_dtype, float k_scale, float v_scale,
+                                  int num_threads) {
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks < 0 || !orc_dtype_ok(q_dtype) || !orc_dtype_ok(kv_dtype))
     return ORC_ERR_ARG;
@@ -224,7 +249,7 @@ int oracle_paged_decode_attention(double* out, const void* q, const void* k_cach
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
     const int32_t* row = block_tables + (size_t)b * max_blocks;
     if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
-                   kv_dtype) != 0) {
+                   kv_dtype, (double)k_scale, (double)v_scale) != 0) {
       for (int j = 0; j < group; ++j)
         for (int d = 0; d < D; ++d)
           out[((size_t)b * H + (size_t)hk * group + j) * D + d] = NAN;
@@ -279,7 +304,7 @@ int oracle_attention_partial(double* m_out, double* l_out, double* o_out, const 
   double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
   const int32_t* row = block_tables + (size_t)b * max_blocks;
   if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
-                 kv_dtype) != 0) {
+                 kv_dtype, 1.0, 1.0) != 0) {
     free(Kc);
     free(Vc);
     return ORC_ERR_DATA;

@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-ORC_F32, ORC_BF16 = 0, 1
+ORC_F32, ORC_BF16, ORC_FP8_E4M3 = 0, 1, 2
 ORC_OK, ORC_ERR_ARG, ORC_ERR_DATA = 0, 1, 4
 
 _lock = threading.Lock()
@@ -56,7 +56,9 @@ def load(path: str | None = None):
         lib.oracle_kv_unpack_blocks.argtypes = [P, P, P, P, I, I, I, I, I, I]
         lib.oracle_kv_unpack_blocks.restype = I
         lib.oracle_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F,
-                                                      I, I, I]
+                                                      I, I, F, F, I]
+        lib.oracle_decode_e4m3.argtypes = [I]
+        lib.oracle_decode_e4m3.restype = ctypes.c_double
         lib.oracle_paged_decode_attention.restype = I
         lib.oracle_attention_partial.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                                  I, F, I, I]
@@ -73,7 +75,10 @@ def _dtype_code(a: np.ndarray) -> int:
         return ORC_F32
     if a.dtype == np.uint16:
         return ORC_BF16
-    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits) arrays, got {a.dtype}")
+    if a.dtype == np.uint8:
+        return ORC_FP8_E4M3
+    raise TypeError("oracle takes float32, uint16 (bf16 bits) or uint8 (FP8 E4M3 codes) "
+                    f"arrays, got {a.dtype}")
 
 
 def _ptr(a: np.ndarray):
@@ -113,9 +118,16 @@ def kv_unpack_blocks(packed, k_cache, v_cache, block_table_row, context_len: int
                                        NB, _dtype_code(k_cache))
 
 
+def decode_e4m3(code: int, lib=None) -> float:
+    """Exact value of one FP8 E4M3 code."""
+    return (lib or load()).oracle_decode_e4m3(int(code))
+
+
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           num_threads: int = 0, lib=None):
-    """fp64 decode attention over the paged cache; returns (out[B,H,D] float64, status)."""
+                           num_threads: int = 0, lib=None, k_scale: float = 1.0,
+                           v_scale: float = 1.0):
+    """fp64 decode attention over the paged cache; returns (out[B,H,D] float64, status).
+    FP8 caches (uint8 codes) mean code value times k_scale / v_scale."""
     lib = lib or load()
     B, H, D = q.shape
     NB, bs, H_kv, D2 = k_cache.shape
@@ -127,7 +139,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     st = lib.oracle_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), max_blocks, _ptr(cl), B, H,
         H_kv, D, bs, NB, ctypes.c_float(scale), _dtype_code(q), _dtype_code(k_cache),
-        int(num_threads))
+        ctypes.c_float(k_scale), ctypes.c_float(v_scale), int(num_threads))
     return out, st
 
 

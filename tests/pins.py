@@ -20,7 +20,10 @@ Facts used:
   - output is linear in V;
   - append then pack gives back the history plus the new token, bit for bit;
   - unpack into freshly scattered blocks then pack gives back the buffer, bit for bit, and
-    unpack touches no row outside the request's tokens.
+    unpack touches no row outside the request's tokens;
+  - every FP8 E4M3 code decodes to the value torch's own float8_e4m3fn conversion gives,
+    and to hand-derived values at the format's landmarks; FP8 attention with per-tensor
+    scales matches the dense brute force run on torch-decoded, scaled values.
 """
 from __future__ import annotations
 
@@ -313,6 +316,62 @@ def pin_unpack_then_pack_roundtrip(lib):
                                   packed[t, 0].view(np.uint8))
             assert np.array_equal(vc[table[t // bs], t % bs].view(np.uint8),
                                   packed[t, 1].view(np.uint8))
+
+
+def pin_e4m3_decode(lib):
+    import torch
+
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([orc.decode_e4m3(c, lib=lib) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    # landmarks of the format, derived by hand
+    hand = {0x00: 0.0, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0x08: 2.0 ** -6,
+            0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in hand.items():
+        assert orc.decode_e4m3(c, lib=lib) == v, hex(c)
+    assert np.isnan(orc.decode_e4m3(0x7F, lib=lib)) and np.isnan(orc.decode_e4m3(0xFF, lib=lib))
+    assert np.signbit(orc.decode_e4m3(0x80, lib=lib))
+
+
+def _fp8_codes(rng, shape):
+    """Random E4M3 codes, NaN codes excluded."""
+    c = rng.integers(0, 254, size=shape).astype(np.uint8)
+    c[c == 0x7F] = 0x7E
+    return c
+
+
+def pin_fp8_attention_brute_force(lib):
+    import torch
+
+    rng = np.random.default_rng(23)
+    for lengths, H, H_kv, D, bs in (([1, 9, 33, 70], 4, 2, 16, 8), ([5, 40], 8, 1, 32, 16)):
+        B = len(lengths)
+        k_scale, v_scale = float(np.float32(0.0123)), float(np.float32(0.031))
+        nblk = [(L + bs - 1) // bs for L in lengths]
+        NB = sum(nblk) + 2
+        kc = _fp8_codes(rng, (NB, bs, H_kv, D))
+        vc = _fp8_codes(rng, (NB, bs, H_kv, D))
+        perm = rng.permutation(NB).astype(np.int32)
+        bt = np.full((B, max(nblk)), -1, np.int32)
+        off = 0
+        for b, n in enumerate(nblk):
+            bt[b, :n] = perm[off:off + n]
+            off += n
+        q = as_stored(rng.standard_normal((B, H, D)), "bf16")
+        scale = float(np.float32(1.0 / math.sqrt(D)))
+        out, st = orc.paged_decode_attention(q, kc, vc, bt, np.array(lengths, np.int32), scale,
+                                             lib=lib, k_scale=k_scale, v_scale=v_scale)
+        assert st == orc.ORC_OK
+        dec = lambda a: torch.from_numpy(a).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        for b, L in enumerate(lengths):
+            rows = [(bt[b, t // bs], t % bs) for t in range(L)]
+            K = np.stack([dec(kc[r]) for r in rows]) * k_scale
+            V = np.stack([dec(vc[r]) for r in rows]) * v_scale
+            ref = brute.dense_decode_attention(stored_to_f64(q[b]), K, V, scale)
+            assert np.abs(out[b] - ref).max() <= 1e-12, (lengths, b)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

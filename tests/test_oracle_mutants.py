@@ -55,6 +55,11 @@ MUTANTS = [
        "((size_t)block * (size_t)block_size + (size_t)((t + 1) % block_size)) * row_bytes;\n    const char* src",
        None)]),
     ("combine_forgets_weights", [("Lsum += l[j] * exp(m[j] - M);", "Lsum += l[j];", None)]),
+    ("e4m3_wrong_bias", [("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)", None)]),
+    ("e4m3_wrong_subnormal", [("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)", None)]),
+    ("kv_scale_dropped",
+     [("Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype) * k_scale;",
+       "Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype);", None)]),
 ]
 
 
