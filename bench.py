@@ -56,13 +56,13 @@ def step_bytes(s, pack_reqs) -> dict:
     pack: the packed requests' K/V read and written, plus their table entries.
     """
     w = s.w
-    e = w.elem_bytes
+    e, e_kv = w.elem_bytes, w.kv_elem_bytes
     L = s.context_lens_np.astype(np.int64)
     bs = w.block_size
     nblk = (L + bs - 1) // bs
-    kv_tok = 2 * w.H_kv * w.D * e
+    kv_tok = 2 * w.H_kv * w.D * e_kv
     attn = int(L.sum()) * kv_tok + 2 * s.B * w.H * w.D * e + int(nblk.sum()) * 4 + s.B * 4
-    append = 2 * s.B * 2 * w.H_kv * w.D * e + s.B * 4
+    append = 2 * s.B * 2 * w.H_kv * w.D * e_kv + s.B * 4
     pl = np.array([int(L[r]) for r in pack_reqs], np.int64)
     pack = int(pl.sum()) * kv_tok * 2 + int(((pl + bs - 1) // bs).sum()) * 4
     return {"attention": attn, "append": append, "pack": pack,
@@ -180,6 +180,20 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.sink)
 
 
+def attention(s, out, sm_cap, workspace, error_word=None, stream=None):
+    """One attention call through the C ABI (the FP8 entry point for FP8 caches)."""
+    import paged_decode_attention_02_gb300 as pda
+    if s.w.kv == "fp8":
+        return pda.paged_decode_attention_fp8(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                              s.context_lens, s.max_context_len, s.scale,
+                                              s.k_scale, s.v_scale, sm_cap=sm_cap,
+                                              workspace=workspace, error_word=error_word,
+                                              stream=stream)
+    return pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                      s.context_lens, s.max_context_len, s.scale, sm_cap=sm_cap,
+                                      workspace=workspace, error_word=error_word, stream=stream)
+
+
 # ------------------------------------------------------------------ distributed
 def dist_setup(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -267,9 +281,9 @@ def run_ours(args, ws, rank, local):
 
     out = torch.empty_like(s.q)
     cap = args.sm_cap
-    wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.torch_dtype, cap, dev)
+    wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype, cap, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    packs = [torch.empty((int(s.context_lens_np[r]), 2, w.H_kv, w.D), dtype=w.torch_dtype,
+    packs = [torch.empty((int(s.context_lens_np[r]), 2, w.H_kv, w.D), dtype=w.kv_torch_dtype,
                          device=dev) for r in pack_reqs]
     pack_rows = [s.block_tables[r] for r in pack_reqs]
     pack_lens = [int(s.context_lens_np[r]) for r in pack_reqs]
@@ -281,9 +295,7 @@ def run_ours(args, ws, rank, local):
         pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
         if ev:
             ev[1].record(stream)
-        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
-                                   s.context_lens, s.max_context_len, s.scale, sm_cap=cap,
-                                   workspace=wsp, error_word=err)
+        attention(s, out, cap, wsp, error_word=err)
         if ev:
             ev[2].record(stream)
         if pack_reqs:
@@ -388,7 +400,7 @@ def run_ours(args, ws, rank, local):
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": s.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
-                   "block_size": w.block_size, "kv_dtype": w.dtype,
+                   "block_size": w.block_size, "kv_dtype": w.kv or w.dtype,
                    "context_tokens": nb["tokens"], "pack_requests": len(pack_reqs),
                    "sm_cap": cap, "parallelism": f"replicas x{ws}",
                    "l2": f"flushed before every step: wrote, then read, a {2 * l2 >> 20} MiB "
@@ -446,7 +458,10 @@ def sweep_workloads(args, dev, flush, peak):
     out_all = {}
     sms = pda.device_sm_count()
     stream = torch.cuda.current_stream(dev)
-    for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128"):
+    for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
+                 "gqa_skew_b256_fp8"):
+        if name == args.config:
+            continue
         w = wl.get(name)
         s = wl.make_step(w, device=dev)
         nb = step_bytes(s, [])
@@ -454,21 +469,17 @@ def sweep_workloads(args, dev, flush, peak):
         res_w = {}
         for cap in caps:
             out = torch.empty_like(s.q)
-            wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.torch_dtype, cap,
-                                      dev)
+            wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype,
+                                      cap, dev)
             for _ in range(3):
                 flush()
-                pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
-                                           s.context_lens, s.max_context_len, s.scale,
-                                           sm_cap=cap, workspace=wsp)
+                attention(s, out, cap, wsp)
             ts = []
             for _ in range(args.sweep_iters):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 flush()
                 a.record(stream)
-                pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
-                                           s.context_lens, s.max_context_len, s.scale,
-                                           sm_cap=cap, workspace=wsp)
+                attention(s, out, cap, wsp)
                 b.record(stream)
                 ts.append((a, b))
             torch.cuda.synchronize()
@@ -627,7 +638,7 @@ def run_reference(args, ws, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "B": sample.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
-                   "block_size": w.block_size, "kv_dtype": w.dtype,
+                   "block_size": w.block_size, "kv_dtype": w.kv or w.dtype,
                    "context_tokens": sb["tokens"], "pack_requests": len(sample.pack_requests)},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{w.name} recipe with B={sample.B} of {w.B} requests "

@@ -52,7 +52,10 @@ typedef enum {
   PDA_ERR_TOO_LARGE = 5    /* needs more scratch than pda_paged_decode_attention_noalloc has */
 } pda_status;
 
-typedef enum { PDA_F32 = 0, PDA_BF16 = 1 } pda_dtype;
+/* Element types. PDA_FP8_E4M3 (the OCP 8-bit format without infinities) is a KV-cache type
+ * only: append, pack and unpack copy its bytes, and pda_paged_decode_attention_fp8 reads it
+ * with per-tensor scales. */
+typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2 } pda_dtype;
 
 /* Bits OR-ed into *error_word by the kernels. */
 #define PDA_DEVERR_CONTEXT_LEN 0x1 /* context_lens[b] < 0, > max_context_len or > table capacity */
@@ -124,7 +127,8 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  *
  *  out            [B, H, D] in out_dtype (PDA_F32 or PDA_BF16).
  *  q              [B, H, D] in q_dtype; q_dtype must equal kv_dtype.
- *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype; read only.
+ *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype (PDA_F32 or PDA_BF16; an
+ *                 FP8 cache goes through pda_paged_decode_attention_fp8); read only.
  *  block_tables   [B, max_blocks_per_seq] int32.
  *  context_lens   [B] int32 (device): tokens of history including this step's token.
  *                 L == 0 gives a zero row. L < 0, L > max_context_len or
@@ -154,6 +158,33 @@ pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_ca
                                       pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype,
                                       int sm_cap, void* workspace, size_t workspace_bytes,
                                       int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_paged_decode_attention_fp8 -- pda_paged_decode_attention over an FP8 E4M3 KV cache.
+ *
+ * A quantised KV cache cuts the bytes each decode step must read (page "From
+ * PagedAttention to Prefill-Decode disaggregation", sec. 6.2: a low-precision KV cache,
+ * dequantised to FP8 before attention, raises memory bandwidth and throughput). Each
+ * stored K code means decode(code) * k_scale and each V code decode(code) * v_scale
+ * (per-tensor scales); the result is softmax(scale * q K^T) V over those values, exactly as
+ * pda_paged_decode_attention computes it. Codes are widened exactly in registers and all
+ * arithmetic is fp32.
+ *
+ *  k_cache, v_cache [num_blocks, block_size, H_kv, D] bytes (E4M3 codes).
+ *  q               [B, H, D] in q_dtype, which must be PDA_BF16.
+ *  k_scale, v_scale finite per-tensor scales.
+ *  Every other argument, the workspace (pda_attention_workspace_size with PDA_FP8_E4M3),
+ *  the supported sizes and the errors are those of pda_paged_decode_attention.
+ */
+pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int max_context_len, int B, int H, int H_kv, int D,
+                                          int block_size, int num_blocks, float scale,
+                                          float k_scale, float v_scale, pda_dtype q_dtype,
+                                          pda_dtype out_dtype, int sm_cap, void* workspace,
+                                          size_t workspace_bytes, int32_t* error_word,
+                                          cudaStream_t stream);
 
 /*
  * pda_paged_decode_attention_noalloc -- pda_paged_decode_attention without a workspace

@@ -6,9 +6,10 @@ The computation lives in ``libpda.so`` (CUDA kernels behind the C ABI of ``inclu
 from .binding import (PdaError, alloc_workspace, attention_workspace_size, device_sm_count,
                       kv_append, kv_pack_blocks, kv_pack_blocks_batched, kv_unpack_blocks,
                       kv_unpack_blocks_batched, paged_decode_attention,
+                      paged_decode_attention_fp8,
                       paged_decode_attention_noalloc, status_string)
 
 __all__ = ["PdaError", "alloc_workspace", "attention_workspace_size", "device_sm_count",
            "kv_append", "kv_pack_blocks", "kv_pack_blocks_batched", "kv_unpack_blocks",
-           "kv_unpack_blocks_batched", "paged_decode_attention", "paged_decode_attention_noalloc",
+           "kv_unpack_blocks_batched", "paged_decode_attention", "paged_decode_attention_fp8", "paged_decode_attention_noalloc",
            "status_string"]

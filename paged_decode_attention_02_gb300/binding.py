@@ -17,7 +17,7 @@ from . import build_lib
 
 (PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE,
  PDA_ERR_TOO_LARGE) = range(6)
-PDA_F32, PDA_BF16 = 0, 1
+PDA_F32, PDA_BF16, PDA_FP8_E4M3 = 0, 1, 2
 PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PDA_PACK_MAX_BATCH = 64
 PDA_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -26,7 +26,7 @@ EXPORTED = [
     "pda_status_string", "pda_version", "pda_device_sm_count", "pda_kv_append",
     "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
     "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
-    "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched",
+    "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched", "pda_paged_decode_attention_fp8",
 ]
 
 _lock = threading.Lock()
@@ -66,6 +66,9 @@ def load():
         lib.pda_paged_decode_attention.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, F,
                                                    I, I, I, I, P, SZ, P, P]
         lib.pda_paged_decode_attention.restype = I
+        lib.pda_paged_decode_attention_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I,
+                                                       F, F, F, I, I, I, P, SZ, P, P]
+        lib.pda_paged_decode_attention_fp8.restype = I
         lib.pda_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I,
                                                            I, I, F, I, I, I, I, P, P]
         lib.pda_paged_decode_attention_noalloc.restype = I
@@ -91,11 +94,14 @@ def _check(status: int, what: str):
 
 
 def _dtype(t: torch.Tensor) -> int:
+    """float32, bfloat16, or FP8 E4M3 codes (torch.float8_e4m3fn, or uint8 holding codes)."""
     if t.dtype == torch.float32:
         return PDA_F32
     if t.dtype == torch.bfloat16:
         return PDA_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PDA_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32, bfloat16 or FP8 E4M3 codes")
 
 
 def _ptr(t: torch.Tensor | None):
@@ -133,7 +139,8 @@ def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, error_word=None, str
 def attention_workspace_size(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat16,
                              sm_cap=0) -> int:
     n = ctypes.c_size_t(0)
-    dt = PDA_BF16 if kv_dtype == torch.bfloat16 else PDA_F32
+    dt = {torch.bfloat16: PDA_BF16, torch.float32: PDA_F32, torch.uint8: PDA_FP8_E4M3,
+          torch.float8_e4m3fn: PDA_FP8_E4M3}[kv_dtype]
     _check(load().pda_attention_workspace_size(B, H, H_kv, D, block_size, dt, sm_cap,
                                                ctypes.byref(n)), "pda_attention_workspace_size")
     return n.value
@@ -141,6 +148,7 @@ def attention_workspace_size(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat
 
 def alloc_workspace(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat16, sm_cap=0,
                     device=None) -> torch.Tensor:
+    """Workspace for one attention call (torch.uint8 / float8_e4m3fn mean an FP8 cache)."""
     n = attention_workspace_size(B, H, H_kv, D, block_size, kv_dtype, sm_cap)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
@@ -162,6 +170,28 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         _dtype(q), _dtype(k_cache), _dtype(out), int(sm_cap), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
         "pda_paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables, context_lens,
+                               max_context_len: int, scale: float, k_scale: float,
+                               v_scale: float, sm_cap: int = 0, workspace=None, error_word=None,
+                               stream=None):
+    """Attention over an FP8 E4M3 cache: stored code c of K means decode(c) * k_scale."""
+    B, H, D = q.shape
+    NB, bs, H_kv, D2 = k_cache.shape
+    assert D == D2 and v_cache.shape == k_cache.shape and out.shape == q.shape
+    assert _dtype(k_cache) == PDA_FP8_E4M3 and _dtype(v_cache) == PDA_FP8_E4M3
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    if workspace is None:
+        workspace = alloc_workspace(B, H, H_kv, D, bs, torch.uint8, sm_cap, q.device)
+    _check(load().pda_paged_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
+        _ptr(context_lens), int(max_context_len), B, H, H_kv, D, bs, NB, float(scale),
+        float(k_scale), float(v_scale), _dtype(q), _dtype(out), int(sm_cap), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
+        "pda_paged_decode_attention_fp8")
     return out
 
 

@@ -69,6 +69,7 @@ struct AttnParams {
   unsigned long long* ws_arrive;  // [B * H_kv] piece arrivals: call number << 16 | count
   unsigned long long call;        // this call's number (48 bits)
   int32_t* error_word;
+  float v_scale;                  // value of a stored V element = code * v_scale (1 if plain)
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
   int out_bf16;
   float scale_log2;
@@ -109,7 +110,7 @@ struct ReduceScatter {
   }
 };
 
-template <typename KV, int D, int G>
+template <typename KV, typename QT, int D, int G>
 struct Geometry {
   using E = Elem<KV>;
   static constexpr int VEC = E::kVec;               // elements per lane per row (16 bytes)
@@ -123,7 +124,7 @@ struct Geometry {
   // Scores of two token slots share one packed fp32x2 FMA when q fits twice in registers.
   static constexpr bool PAIR_QK = G * VEC <= 32 && TPL % 2 == 0;
   static constexpr uint32_t TILE_BYTES = kBS * D * sizeof(KV);
-  static constexpr uint32_t Q_BYTES = G * D * sizeof(KV);
+  static constexpr uint32_t Q_BYTES = G * D * sizeof(QT);
   static_assert(32 % LPR == 0 && kBS % RPW == 0, "row geometry");
   static_assert(LPR >= G, "one head per lane after the reduce-scatter");
   static_assert(VEC % 2 == 0, "packed fp32x2 accumulation");
@@ -137,9 +138,9 @@ struct Geometry {
 // forms N = G * TPL partial dot products (head j, slot i; real index j * TPL + i), sums
 // them with the other lanes of its row group by a reduce-scatter, and is left with C
 // complete scores of one head: real indices idx0 .. idx0 + C - 1.
-template <typename KV, int D, int G>
+template <typename KV, typename QT, int D, int G>
 struct WarpAttn {
-  using Geo = Geometry<KV, D, G>;
+  using Geo = Geometry<KV, QT, D, G>;
   using E = typename Geo::E;
   static constexpr int VEC = Geo::VEC, LPR = Geo::LPR, RPW = Geo::RPW, TPL = Geo::TPL;
   static constexpr int N = Geo::N, C = Geo::C, DUP = Geo::DUP, LPH = Geo::LPH;
@@ -165,11 +166,11 @@ struct WarpAttn {
     for (int il = 0; il < TPL; ++il) krow[il] = (rw + RPW * (il ^ tp)) * D + cl * VEC;
   }
 
-  __device__ __forceinline__ void reset(const KV* q_smem, float scale_log2) {
+  __device__ __forceinline__ void reset(const QT* q_smem, float scale_log2) {
 #pragma unroll
     for (int jl = 0; jl < G; ++jl) {
       float t[VEC];
-      E::load16(q_smem + (jl ^ hp) * D + cl * VEC, t);
+      load_elems<QT, VEC>(q_smem + (jl ^ hp) * D + cl * VEC, t);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float qv = t[e] * scale_log2;
@@ -195,8 +196,8 @@ struct WarpAttn {
 #pragma unroll
       for (int m = 0; m < TPL / 2; ++m) {
         float k0[VEC], k1[VEC];
-        E::load16(ks + krow[2 * m], k0);
-        E::load16(ks + krow[2 * m + 1], k1);
+        E::load(ks + krow[2 * m], k0);
+        E::load(ks + krow[2 * m + 1], k1);
 #pragma unroll
         for (int jl = 0; jl < G; ++jl) {
           float2 acc = __fmul2_rn(q2[jl][0], make_float2(k0[0], k1[0]));
@@ -211,7 +212,7 @@ struct WarpAttn {
 #pragma unroll
       for (int il = 0; il < TPL; ++il) {
         float k[VEC];
-        E::load16(ks + krow[il], k);
+        E::load(ks + krow[il], k);
 #pragma unroll
         for (int jl = 0; jl < G; ++jl) {
           float acc = qs[jl][0] * k[0];
@@ -264,7 +265,7 @@ struct WarpAttn {
     for (int i = 0; i < TPL; ++i) {
       const int t = rw + RPW * i;
       float v[VEC];
-      E::load16(vs + t * D + cl * VEC, v);
+      E::load(vs + t * D + cl * VEC, v);
       if (kPartial && t >= n_valid) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[e] = 0.f;
@@ -428,7 +429,7 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
     const size_t row = (static_cast<size_t>(b) * p.H + static_cast<size_t>(h) * G + j0 + j) * D;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      const float v = acc[j][e] / Lsum[j];
+      const float v = acc[j][e] * (p.v_scale / Lsum[j]);
       if (p.out_bf16)
         reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
       else
@@ -447,12 +448,12 @@ __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1,
     merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, W_tiles, NW, lane);
 }
 
-template <typename KV, int D, int G>
+template <typename KV, typename QT, int D, int G>
 __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using Geo = Geometry<KV, D, G>;
-  using W = WarpAttn<KV, D, G>;
+  using Geo = Geometry<KV, QT, D, G>;
+  using W = WarpAttn<KV, QT, D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   if ((smem_addr(smem) & 127u) != 0) {  // TMA destinations below assume 128-byte alignment
     if (threadIdx.x == 0) atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
     return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + Geo::TILE_BYTES);
   };
   auto q_buf = [&](int s) {
-    return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
+    return reinterpret_cast<QT*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
   };
 
   // (request, kv-head, block) of tile y
@@ -616,7 +617,7 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
       tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
       tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
       if (need_q) {
-        const KV* src = reinterpret_cast<const KV*>(p.q) +
+        const QT* src = reinterpret_cast<const QT*>(p.q) +
                         (static_cast<size_t>(cur_b) * p.H + static_cast<size_t>(cur_h) * G) * D;
         bulk_load(q_buf(s), src, Geo::Q_BYTES, &my_bar[s]);
       }
@@ -683,7 +684,7 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             float v[W::VEC];
-            const float inv = seg_bad ? __int_as_float(0x7fc00000) : 1.f / lj[j];
+            const float inv = seg_bad ? __int_as_float(0x7fc00000) : p.v_scale / lj[j];
 #pragma unroll
             for (int e = 0; e < W::VEC; ++e) v[e] = st.o(j, e) * inv;
             const size_t off =
@@ -757,10 +758,13 @@ struct LaunchPlan {
   size_t ws_arrive, ws_ml, ws_o, ws_total;  // byte offsets / total
 };
 
+// q is bf16 beside an FP8 cache, otherwise of the cache's own type.
+size_t q_bytes_for(pda_dtype kv) { return kv == PDA_FP8_E4M3 ? 2u : dtype_bytes(kv); }
+
 uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
-  const uint32_t e = static_cast<uint32_t>(dtype_bytes(kv));
-  const uint32_t tile = kBS * D * e;
-  return 2 * tile + static_cast<uint32_t>(round_up(static_cast<size_t>(G) * D * e, 128));
+  const uint32_t tile = kBS * D * static_cast<uint32_t>(dtype_bytes(kv));
+  return 2 * tile +
+         static_cast<uint32_t>(round_up(static_cast<size_t>(G) * D * q_bytes_for(kv), 128));
 }
 
 bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
@@ -801,24 +805,27 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnParams);
 
-template <typename KV, int D>
+template <typename KV, typename QT, int D>
 KernelFn pick_g(int G) {
   switch (G) {
-    case 1: return attn_partial_kernel<KV, D, 1>;
-    case 2: return attn_partial_kernel<KV, D, 2>;
-    case 4: return attn_partial_kernel<KV, D, 4>;
-    case 8: return attn_partial_kernel<KV, D, 8>;
+    case 1: return attn_partial_kernel<KV, QT, D, 1>;
+    case 2: return attn_partial_kernel<KV, QT, D, 2>;
+    case 4: return attn_partial_kernel<KV, QT, D, 4>;
+    case 8: return attn_partial_kernel<KV, QT, D, 8>;
     default: return nullptr;
   }
 }
 
 KernelFn pick_kernel(pda_dtype kv, int D, int G) {
   if (kv == PDA_BF16) {
-    if (D == 128) return pick_g<__nv_bfloat16, 128>(G);
-    if (D == 64) return pick_g<__nv_bfloat16, 64>(G);
+    if (D == 128) return pick_g<__nv_bfloat16, __nv_bfloat16, 128>(G);
+    if (D == 64) return pick_g<__nv_bfloat16, __nv_bfloat16, 64>(G);
+  } else if (kv == PDA_FP8_E4M3) {
+    if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128>(G);
+    if (D == 64) return pick_g<fp8e4m3, __nv_bfloat16, 64>(G);
   } else {
-    if (D == 128) return pick_g<float, 128>(G);
-    if (D == 64) return pick_g<float, 64>(G);
+    if (D == 128) return pick_g<float, float, 128>(G);
+    if (D == 64) return pick_g<float, float, 64>(G);
   }
   return nullptr;
 }
@@ -902,16 +909,24 @@ extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D
   return PDA_OK;
 }
 
-extern "C" pda_status pda_paged_decode_attention(
-    void* out, const void* q, const void* k_cache, const void* v_cache,
-    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
-    float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
-    void* workspace, size_t workspace_bytes, int32_t* error_word, cudaStream_t stream) {
+namespace pda {
+namespace {
+
+// The attention launch behind every public entry point. kv_dtype selects the cache format;
+// k_scale and v_scale are the values of one stored unit of K and V (1 for plain caches).
+pda_status launch_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len, int B, int H,
+                            int H_kv, int D, int block_size, int num_blocks, float scale,
+                            float k_scale, float v_scale, pda_dtype q_dtype,
+                            pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
+                            void* workspace, size_t workspace_bytes, int32_t* error_word,
+                            cudaStream_t stream) {
   // ---- host-side validation, before any CUDA call
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || sm_cap < 0 ||
-      !dtype_ok(q_dtype) || !dtype_ok(kv_dtype) || !dtype_ok(out_dtype) || !isfinite(scale))
+      !float_dtype_ok(q_dtype) || !dtype_ok(kv_dtype) || !float_dtype_ok(out_dtype) ||
+      !isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale))
     return PDA_ERR_INVALID_ARG;
   if (B == 0) return PDA_OK;
   if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
@@ -920,7 +935,8 @@ extern "C" pda_status pda_paged_decode_attention(
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PDA_ERR_INVALID_ARG;
   const int G = H / H_kv;
-  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(G) || q_dtype != kv_dtype ||
+  const bool q_ok = kv_dtype == PDA_FP8_E4M3 ? q_dtype == PDA_BF16 : q_dtype == kv_dtype;
+  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(G) || !q_ok ||
       B > kMaxBatch)
     return PDA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31) ||
@@ -958,6 +974,7 @@ extern "C" pda_status pda_paged_decode_attention(
   ap.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   ap.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
   ap.error_word = error_word;
+  ap.v_scale = v_scale;
   ap.B = B;
   ap.H = H;
   ap.H_kv = H_kv;
@@ -965,7 +982,8 @@ extern "C" pda_status pda_paged_decode_attention(
   ap.max_blocks = max_blocks_per_seq;
   ap.max_context_len = max_context_len;
   ap.out_bf16 = out_dtype == PDA_BF16;
-  ap.scale_log2 = scale * 1.4426950408889634f;
+  // the K scale folds into q's pre-scale: s = scale * (k_scale * code) . q
+  ap.scale_log2 = scale * k_scale * 1.4426950408889634f;
   ap.num_workers = pl.grid * pl.nwarps;
   ap.stages = pl.stages;
   ap.stage_bytes = pl.stage_bytes;
@@ -973,8 +991,36 @@ extern "C" pda_status pda_paged_decode_attention(
 
   fn<<<pl.grid, pl.nwarps * 32, pl.smem_bytes, stream>>>(tmK, tmV, ap);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
-
   return PDA_OK;
+}
+
+}  // namespace
+}  // namespace pda
+
+extern "C" pda_status pda_paged_decode_attention(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
+    float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
+    void* workspace, size_t workspace_bytes, int32_t* error_word, cudaStream_t stream) {
+  if (kv_dtype == PDA_FP8_E4M3) return PDA_ERR_UNSUPPORTED;  // needs its scales: _fp8 entry
+  return launch_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                          context_lens, max_context_len, B, H, H_kv, D, block_size, num_blocks,
+                          scale, 1.f, 1.f, q_dtype, kv_dtype, out_dtype, sm_cap, workspace,
+                          workspace_bytes, error_word, stream);
+}
+
+extern "C" pda_status pda_paged_decode_attention_fp8(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
+    float scale, float k_scale, float v_scale, pda_dtype q_dtype, pda_dtype out_dtype,
+    int sm_cap, void* workspace, size_t workspace_bytes, int32_t* error_word,
+    cudaStream_t stream) {
+  return launch_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                          context_lens, max_context_len, B, H, H_kv, D, block_size, num_blocks,
+                          scale, k_scale, v_scale, q_dtype, PDA_FP8_E4M3, out_dtype, sm_cap,
+                          workspace, workspace_bytes, error_word, stream);
 }
 
 // ------------------------------------------------------------------ no-allocation variant

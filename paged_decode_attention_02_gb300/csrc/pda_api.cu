@@ -57,8 +57,9 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
                                  static_cast<cuuint64_t>(H_kv) * D * e};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(block_size)};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
-  const CUtensorMapDataType dt =
-      dtype == PDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType dt = dtype == PDA_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == PDA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const CUresult r = g_encode(tm, dt, 3, const_cast<void*>(base), dims, strides, box,
                               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

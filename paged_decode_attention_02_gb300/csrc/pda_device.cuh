@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -136,15 +137,20 @@ __device__ __forceinline__ void atomic_or_error(int32_t* error_word, int32_t bit
 }
 
 // ---------------------------------------------------------------- element access
+// FP8 E4M3 code (the OCP format with no infinities), one byte.
+struct fp8e4m3 {
+  uint8_t bits;
+};
+
 template <typename T>
 struct Elem;
 
+// Each lane moves kVec elements per access; load() widens them exactly to fp32.
 template <>
 struct Elem<float> {
   static constexpr int kBytes = 4;
-  static constexpr int kVec = 4;  // elements per 16-byte access
-  // Loads kVec elements (16 bytes) and widens them to fp32.
-  static __device__ __forceinline__ void load16(const void* p, float* out) {
+  static constexpr int kVec = 4;  // one 16-byte access
+  static __device__ __forceinline__ void load(const void* p, float* out) {
     const float4 v = *reinterpret_cast<const float4*>(p);
     out[0] = v.x;
     out[1] = v.y;
@@ -156,8 +162,8 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kBytes = 2;
-  static constexpr int kVec = 8;
-  static __device__ __forceinline__ void load16(const void* p, float* out) {
+  static constexpr int kVec = 8;  // one 16-byte access
+  static __device__ __forceinline__ void load(const void* p, float* out) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     out[0] = bf16_lo(v.x);
     out[1] = bf16_hi(v.x);
@@ -169,5 +175,41 @@ struct Elem<__nv_bfloat16> {
     out[7] = bf16_hi(v.w);
   }
 };
+
+// Four E4M3 codes in a 32-bit word, widened exactly (E4M3 values are all exact in fp16).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* out) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  out[0] = a.x;
+  out[1] = a.y;
+  out[2] = b.x;
+  out[3] = b.y;
+}
+
+template <>
+struct Elem<fp8e4m3> {
+  static constexpr int kBytes = 1;
+  static constexpr int kVec = 8;  // one 8-byte access (keeps the bf16 lane geometry)
+  static __device__ __forceinline__ void load(const void* p, float* out) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    e4m3x4_to_f32(v.x, out);
+    e4m3x4_to_f32(v.y, out + 4);
+  }
+};
+
+// Loads n elements of type T (n a multiple of Elem<T>::kVec) widened to fp32.
+template <typename T, int n>
+__device__ __forceinline__ void load_elems(const T* p, float* out) {
+  static_assert(n % Elem<T>::kVec == 0, "whole accesses");
+#pragma unroll
+  for (int i = 0; i < n; i += Elem<T>::kVec) Elem<T>::load(p + i, out + i);
+}
 
 }  // namespace pda

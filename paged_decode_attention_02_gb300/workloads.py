@@ -20,6 +20,9 @@ Recipe (one per named workload):
   - q, the pool's K and V, and the appended token's K/V are N(0,1) drawn in fp32 by a
     ``torch.Generator`` seeded from the third stream, on the device the caller asks for,
     then rounded to the workload's dtype (round-to-nearest-even for bf16);
+  - FP8 workloads store E4M3 codes of value / scale (per-tensor scales, K and V apart;
+    torch's float8_e4m3fn rounding), drawn with the seeds of their bf16 twin so the
+    lengths and tables are the same;
   - context lengths count the tokens after this step's append, so the appended token is
     the last position each request attends to; ``slot_mapping[b]`` points at it.
 """
@@ -49,6 +52,10 @@ class Workload:
     pack_top: int = 0  # number of longest requests whose KV is packed each step
     sm_caps_pct: tuple = field(default_factory=tuple)  # SM-fraction sweep, % of SMs
     description: str = ""
+    kv: str = ""  # "" : the cache holds `dtype`; "fp8": FP8 E4M3 codes with per-tensor scales
+    k_scale: float = 1.0  # value of one K code unit (FP8 caches)
+    v_scale: float = 1.0
+    seed_of: int = 0  # draw with another workload's seeds (same lengths and tables)
 
     @property
     def group(self) -> int:
@@ -60,7 +67,16 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
+        """Bytes of one q / out element."""
         return 4 if self.dtype == "f32" else 2
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv == "fp8" else self.elem_bytes
+
+    @property
+    def kv_torch_dtype(self):
+        return torch.uint8 if self.kv == "fp8" else self.torch_dtype
 
 
 WORKLOADS = {
@@ -83,6 +99,14 @@ WORKLOADS = {
                  lengths="uniform:512,2048", pool="scaled:1.25",
                  sm_caps_pct=(10, 20, 40, 60, 100),
                  description="Llama-2-7B shape, batch 128, context U[512,2048], SM-fraction sweep"),
+        Workload("gqa_skew_b256_fp8", 6, B=256, H=32, H_kv=8, D=128, block_size=16,
+                 dtype="bf16", lengths="loguniform:16,32768", pool="scaled:1.25", pack_top=8,
+                 kv="fp8", k_scale=0.03, v_scale=0.05, seed_of=4,
+                 description="gqa_skew_b256 with an FP8 E4M3 KV cache (per-tensor scales)"),
+        Workload("llama2_13b_b80_fp8", 7, B=80, H=40, H_kv=40, D=128, block_size=16,
+                 dtype="bf16", lengths="uniform:128,4096", pool="scaled:1.25", kv="fp8",
+                 k_scale=0.03, v_scale=0.05, seed_of=3,
+                 description="llama2_13b_b80 with an FP8 E4M3 KV cache (per-tensor scales)"),
     ]
 }
 
@@ -98,7 +122,7 @@ def get(name_or_index) -> Workload:
 
 
 def _streams(w: Workload, seed: int | None):
-    ss = np.random.SeedSequence(1000 + w.index if seed is None else seed)
+    ss = np.random.SeedSequence(1000 + (w.seed_of or w.index) if seed is None else seed)
     return ss.spawn(3)
 
 
@@ -146,20 +170,28 @@ class Step:
     slot_mapping: torch.Tensor
     scale: float
     pack_requests: list
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def max_context_len(self) -> int:
         return int(self.context_lens_np.max()) if self.B else 0
 
 
-def _randn(shape, gen: torch.Generator, device, dtype, chunk: int = 1 << 28) -> torch.Tensor:
-    """N(0,1) drawn in fp32 and rounded to dtype, in chunks to bound the fp32 temporary."""
-    out = torch.empty(shape, dtype=dtype, device=device)
+def _randn(shape, gen: torch.Generator, device, dtype, chunk: int = 1 << 28,
+           scale_by: float = 1.0, to=None) -> torch.Tensor:
+    """N(0,1) drawn in fp32, times scale_by, rounded to dtype (or to `to`, stored as raw
+    bytes when `to` is an 8-bit float type), in chunks to bound the fp32 temporary."""
+    store = torch.uint8 if to is not None else dtype
+    out = torch.empty(shape, dtype=store, device=device)
     flat = out.view(-1)
     n = flat.numel()
     for s in range(0, n, chunk):
         e = min(n, s + chunk)
-        flat[s:e] = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32).to(dtype)
+        x = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
+        if scale_by != 1.0:
+            x = x * scale_by
+        flat[s:e] = x.to(to).view(torch.uint8) if to is not None else x.to(dtype)
     return out
 
 
@@ -201,18 +233,29 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
     gen.manual_seed(int(np.random.default_rng(s_val).integers(0, 2**62)))
     dt = w.torch_dtype
     q = _randn((B, w.H, w.D), gen, device, dt)
-    k_cache = _randn((NB, bs, w.H_kv, w.D), gen, device, dt)
-    v_cache = _randn((NB, bs, w.H_kv, w.D), gen, device, dt)
-    k_new = _randn((B, w.H_kv, w.D), gen, device, dt)
-    v_new = _randn((B, w.H_kv, w.D), gen, device, dt)
+    if w.kv == "fp8":
+        # N(0,1) values stored as E4M3 codes of value / scale (round to nearest even)
+        def kvt(shape, sc):
+            return _randn(shape, gen, device, torch.float32, scale_by=1.0 / sc,
+                          to=torch.float8_e4m3fn)
+        k_cache = kvt((NB, bs, w.H_kv, w.D), w.k_scale)
+        v_cache = kvt((NB, bs, w.H_kv, w.D), w.v_scale)
+        k_new = kvt((B, w.H_kv, w.D), w.k_scale)
+        v_new = kvt((B, w.H_kv, w.D), w.v_scale)
+    else:
+        k_cache = _randn((NB, bs, w.H_kv, w.D), gen, device, dt)
+        v_cache = _randn((NB, bs, w.H_kv, w.D), gen, device, dt)
+        k_new = _randn((B, w.H_kv, w.D), gen, device, dt)
+        v_new = _randn((B, w.H_kv, w.D), gen, device, dt)
     if poison_unused:
         valid = np.zeros(NB * bs, bool)
         for b in range(B):
             for t in range(int(L[b])):
                 valid[bt[b, t // bs] * bs + t % bs] = True
         bad = torch.from_numpy(~valid).to(device).view(NB, bs)
-        k_cache[bad] = float("nan")
-        v_cache[bad] = float("nan")
+        nan = 0x7F if w.kv == "fp8" else float("nan")  # 0x7F is the E4M3 NaN code
+        k_cache[bad] = nan
+        v_cache[bad] = nan
 
     order = np.argsort(-L.astype(np.int64), kind="stable")
     pack = [int(b) for b in order[: w.pack_top]] if w.pack_top else []
@@ -225,4 +268,6 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
         slot_mapping=torch.from_numpy(slots).to(device),
         scale=float(np.float32(1.0 / math.sqrt(w.D))),
         pack_requests=pack,
+        k_scale=float(np.float32(w.k_scale)),
+        v_scale=float(np.float32(w.v_scale)),
     )

@@ -63,7 +63,8 @@ def oracle_full_step(s, append: bool = True, num_threads: int = 0):
     if append:
         assert orc.kv_append(to_np(s.k_new), to_np(s.v_new), kc, vc, s.slot_mapping_np) == 0
     ref, st = orc.paged_decode_attention(to_np(s.q), kc, vc, s.block_tables_np,
-                                         s.context_lens_np, s.scale, num_threads=num_threads)
+                                         s.context_lens_np, s.scale, num_threads=num_threads,
+                                         k_scale=s.k_scale, v_scale=s.v_scale)
     return ref, st, kc, vc
 
 
@@ -93,7 +94,8 @@ def oracle_sampled(s, reqs, append: bool = True):
         st = orc.kv_append(to_np(s.k_new[reqs]), to_np(s.v_new[reqs]), kc, vc, slots)
         assert st == 0
     q = to_np(s.q[reqs]).copy()
-    ref, st = orc.paged_decode_attention(q, kc, vc, bt, lens, s.scale)
+    ref, st = orc.paged_decode_attention(q, kc, vc, bt, lens, s.scale, k_scale=s.k_scale,
+                                         v_scale=s.v_scale)
     return ref, st
 
 
@@ -103,8 +105,14 @@ def gpu_step(s, append: bool = True, sm_cap: int = 0, out_dtype=None, workspace=
     if append:
         pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
     out = torch.empty(s.q.shape, dtype=out_dtype or s.q.dtype, device=s.q.device)
-    pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables, s.context_lens,
-                               s.max_context_len, s.scale, sm_cap=sm_cap, workspace=workspace,
-                               error_word=err)
+    if s.k_cache.dtype == torch.uint8:
+        pda.paged_decode_attention_fp8(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                       s.context_lens, s.max_context_len, s.scale, s.k_scale,
+                                       s.v_scale, sm_cap=sm_cap, workspace=workspace,
+                                       error_word=err)
+    else:
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                   s.context_lens, s.max_context_len, s.scale, sm_cap=sm_cap,
+                                   workspace=workspace, error_word=err)
     torch.cuda.synchronize()
     return out, int(err.item())

@@ -414,3 +414,72 @@ def test_unpack_bad_block_is_skipped_with_error_bit():
     bt = s.block_tables[b].cpu().numpy()
     orc.kv_unpack_blocks(to_np(buf), kc, vc, bt, L)  # the oracle skips the same tokens
     assert np.array_equal(to_np(s.k_cache), kc)
+
+
+
+# ------------------------------------------------------------------ FP8 E4M3 KV cache
+FP8_SHAPES = [(128, 32, 32), (128, 32, 16), (128, 32, 8), (128, 32, 4), (64, 16, 16),
+              (64, 16, 4)]
+
+
+@pytest.mark.parametrize("D,H,H_kv", FP8_SHAPES)
+def test_fp8_shapes_and_groups(D, H, H_kv):
+    w = variant("llama2_13b_b80_fp8", D=D, H=H, H_kv=H_kv, B=9, lengths="uniform:1,700")
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, 700, 255], np.int32)
+    s = wl.make_step(w, device=DEV, lengths=lens)
+    ref, st, kc, vc = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
+    assert_attention_close(out, ref, f"fp8 D={D} H={H} H_kv={H_kv}")
+
+
+@pytest.mark.parametrize("name,B", [("llama2_13b_b80_fp8", 10), ("gqa_skew_b256_fp8", 24)])
+def test_fp8_reduced_batch_every_output(name, B):
+    s = wl.make_step(name, device=DEV, B=B)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, name, strict=True)
+
+
+def test_fp8_full_size_sampled_and_pack():
+    s = wl.make_step("gqa_skew_b256_fp8", device=DEV)
+    reqs = _sample(s)
+    ref, st = oracle_sampled(s, reqs)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out[reqs], ref, "gqa_skew_b256_fp8", strict=True)
+    r = s.pack_requests[0]
+    L = int(s.context_lens_np[r])
+    packed = torch.empty((L, 2, s.w.H_kv, s.w.D), dtype=torch.uint8, device=DEV)
+    pda.kv_pack_blocks(packed, s.k_cache, s.v_cache, s.block_tables[r], L)
+    n = (L + 15) // 16
+    blocks = torch.from_numpy(s.block_tables_np[r, :n].astype(np.int64)).to(DEV)
+    want, st = orc.kv_pack_blocks(to_np(s.k_cache.index_select(0, blocks)).copy(),
+                                  to_np(s.v_cache.index_select(0, blocks)).copy(),
+                                  np.arange(n, dtype=np.int32), L)
+    assert st == 0 and np.array_equal(to_np(packed), want)
+
+
+def test_fp8_empty_single_and_poisoned_rows():
+    lens = np.array([0, 1, 2, 16, 17, 40], np.int32)
+    s = wl.make_step("llama2_13b_b80_fp8", device=DEV, lengths=lens, B=6, poison_unused=True)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0 and np.isfinite(ref).all()
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert_attention_close(out, ref, "fp8 edge cases")
+    assert (out[0] == 0).all()
+
+
+def test_fp8_entry_rejects_plain_caches_and_base_entry_rejects_fp8():
+    s = wl.make_step("llama2_13b_b80_fp8", device=DEV, B=2)
+    out = torch.empty_like(s.q)
+    with pytest.raises(binding.PdaError) as e:
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
+                                   s.context_lens, s.max_context_len, s.scale)
+    assert e.value.status == binding.PDA_ERR_UNSUPPORTED

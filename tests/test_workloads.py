@@ -6,9 +6,19 @@ import torch
 from paged_decode_attention_02_gb300 import workloads as wl
 
 
-def test_five_named_workloads():
-    assert [wl.get(i).name for i in range(1, 6)] == [
-        "tiny", "llama2_7b_b8", "llama2_13b_b80", "gqa_skew_b256", "sm_sweep_b128"]
+def test_named_workloads():
+    assert [wl.get(i).name for i in range(1, 8)] == [
+        "tiny", "llama2_7b_b8", "llama2_13b_b80", "gqa_skew_b256", "sm_sweep_b128",
+        "gqa_skew_b256_fp8", "llama2_13b_b80_fp8"]
+
+
+def test_fp8_workload_shares_lengths_and_tables_with_its_twin():
+    a = wl.make_step("gqa_skew_b256_fp8", B=3)
+    b = wl.make_step("gqa_skew_b256", B=3)
+    assert np.array_equal(a.context_lens_np, b.context_lens_np)
+    assert np.array_equal(a.block_tables_np, b.block_tables_np)
+    assert a.k_cache.dtype == torch.uint8 and a.q.dtype == torch.bfloat16
+    assert not (a.k_cache == 0x7F).any() and not (a.k_cache == 0xFF).any()  # no NaN codes
 
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
