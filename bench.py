@@ -210,13 +210,21 @@ def dist_setup(args):
 
 
 def dist_max(x: float, ws: int) -> float:
+    """The largest of every rank's x (the slowest rank's time decides a replica run)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(bytes_per_step: float, t_step_max: float, ws: int) -> float:
+    """Whole-job GB/s of N independent replicas: every rank moved bytes_per_step in each
+    step, and the job's step time is the slowest rank's."""
+    return ws * bytes_per_step / t_step_max / 1e9
 
 
 def barrier(ws):
@@ -388,7 +396,7 @@ def run_ours(args, ws, rank, local):
     traffic = profiled_traffic(w.name) if (args.batch is None and cap == 0) else None
     res = {
         "metric": METRIC,
-        "value": round(ws * nb["step"] / t_step_max / 1e9, 2),
+        "value": round(replica_value(nb["step"], t_step_max, ws), 2),
         "unit": "GB/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -421,7 +429,7 @@ def run_ours(args, ws, rank, local):
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
                      "traffic": traffic, "kernel": "paged_decode_attention call "
                      "(attn_partial_kernel + attn_combine_kernel)", "peak_source": peak_src},
-        "e2e": {"value": round(ws * nb["step"] / t_e2e / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(replica_value(nb["step"], t_e2e, ws), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -439,12 +447,15 @@ def run_ours(args, ws, rank, local):
         while t_cpu < args.cpu_seconds or reps == 0:
             t_cpu += oracle_pass(sample, threads)
             reps += 1
+        t_one = oracle_pass(sample, 1)  # the same sample on one core
         res["cpu_baseline"] = {
             "value": round(sb["step"] * reps / t_cpu / 1e9, 4), "unit": "GB/s",
             "cores": threads, "kind": "oracle",
+            "value_one_core": round(sb["step"] / t_one / 1e9, 4),
             "sample": f"{w.name} recipe with B={sample.B} ({sb['tokens']} tokens, pack of "
-                      f"{len(sample.pack_requests)}), fp64 C oracle, {reps} pass(es), "
-                      f"{t_cpu:.1f} s"}
+                      f"{len(sample.pack_requests)}), fp64 C oracle, {reps} pass(es) on "
+                      f"{threads} threads in {t_cpu:.1f} s; one pass on 1 thread in "
+                      f"{t_one:.1f} s"}
     return res
 
 

@@ -3,13 +3,13 @@
 The computation lives in ``libpda.so`` (CUDA kernels behind the C ABI of ``include/pda.h``);
 ``binding`` marshals torch tensors into it and ``workloads`` draws seeded synthetic inputs.
 """
-from .binding import (PdaError, alloc_workspace, attention_workspace_size, device_sm_count,
+from .binding import (PdaDeviceError, PdaError, alloc_workspace, check_error, attention_workspace_size, device_sm_count,
                       kv_append, kv_pack_blocks, kv_pack_blocks_batched, kv_unpack_blocks,
                       kv_unpack_blocks_batched, paged_decode_attention,
                       paged_decode_attention_fp8,
                       paged_decode_attention_noalloc, status_string)
 
-__all__ = ["PdaError", "alloc_workspace", "attention_workspace_size", "device_sm_count",
+__all__ = ["PdaDeviceError", "PdaError", "alloc_workspace", "check_error", "attention_workspace_size", "device_sm_count",
            "kv_append", "kv_pack_blocks", "kv_pack_blocks_batched", "kv_unpack_blocks",
            "kv_unpack_blocks_batched", "paged_decode_attention", "paged_decode_attention_fp8", "paged_decode_attention_noalloc",
            "status_string"]

@@ -88,6 +88,31 @@ def status_string(status: int) -> str:
     return load().pda_status_string(int(status)).decode()
 
 
+class PdaDeviceError(RuntimeError):
+    """A kernel reported bad device data (or a timed-out wait) through the error word."""
+
+    NAMES = {PDA_DEVERR_CONTEXT_LEN: "context length out of range",
+             PDA_DEVERR_BLOCK_ID: "block id out of range",
+             PDA_DEVERR_SLOT: "slot out of range",
+             PDA_DEVERR_TIMEOUT: "pipeline wait timed out"}
+
+    def __init__(self, bits: int):
+        self.bits = bits
+        names = [n for b, n in self.NAMES.items() if bits & b] or [f"bits {bits:#x}"]
+        super().__init__("device error: " + ", ".join(names))
+
+
+def check_error(error_word: torch.Tensor, reset: bool = True):
+    """Synchronises, reads a device error word and raises PdaDeviceError if any bit is set
+    (and, by default, zeroes it). A host sync: for tests and debugging, not the hot loop."""
+    torch.cuda.synchronize(error_word.device)
+    bits = int(error_word.item())
+    if reset:
+        error_word.zero_()
+    if bits:
+        raise PdaDeviceError(bits)
+
+
 def _check(status: int, what: str):
     if status != PDA_OK:
         raise PdaError(status, what)
