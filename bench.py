@@ -266,6 +266,27 @@ def oracle_sample(w, seconds: float, threads: int):
     return probe if B == probe_B else wl.make_step(w, device="cpu", B=B)
 
 
+def oracle_legs(w, seconds: float = 2.0, max_B: int = 12) -> dict:
+    """The fp64 oracle on a bounded sample of workload w (its first max_B requests, drawn by
+    the same recipe on the host): all host cores, repeated for about `seconds`, and one
+    pass on one core."""
+    from paged_decode_attention_02_gb300 import workloads as wl
+
+    threads = cpu_threads()
+    sample = wl.make_step(w, device="cpu", B=min(w.B, max_B))
+    b = step_bytes(sample, sample.pack_requests)
+    reps, t = 0, 0.0
+    while t < seconds or reps == 0:
+        t += oracle_pass(sample, threads)
+        reps += 1
+    t1 = oracle_pass(sample, 1)
+    return {"sample": f"B={sample.B} ({b['tokens']} tokens)",
+            "all_cores": {"GBps": round(b["step"] * reps / t / 1e9, 4), "threads": threads,
+                          "s_per_pass": round(t / reps, 3)},
+            "one_core": {"GBps": round(b["step"] / t1 / 1e9, 4), "threads": 1,
+                         "s_per_pass": round(t1, 3)}}
+
+
 def cpu_threads() -> int:
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
@@ -501,6 +522,8 @@ def sweep_workloads(args, dev, flush, peak):
                           "frac_of_peak": round(gbs / peak, 4),
                           "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
         res_w["bytes"] = nb["attention"]
+        if not args.no_cpu_baseline:
+            res_w["oracle"] = oracle_legs(w)
         if name == "llama2_7b_b8":
             res_w["host_overhead_per_layer"] = graph_legs(args, s, sms)
         if w.sm_caps_pct:
