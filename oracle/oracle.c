@@ -52,7 +52,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8_E4M3 = 2, ORC_NVFP4 = 3 };
 enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_DATA = 4 };
 
 static size_t orc_elem_size(int dtype) {
@@ -76,6 +76,19 @@ static double orc_e4m3(uint8_t c) {
 }
 
 double oracle_decode_e4m3(int code) { return orc_e4m3((uint8_t)(code & 255)); }
+
+/*
+ * FP4 E2M1: sign bit, 2 exponent bits with bias 1, 1 mantissa bit. Exponent 0 encodes the
+ * subnormals 0 and 0.5; otherwise (1 + m/2) * 2^(e - 1). Magnitudes 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6; no infinities or NaN.
+ */
+static double orc_e2m1(unsigned code) {
+  const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -mag : mag;
+}
+
+double oracle_decode_e2m1(int code) { return orc_e2m1((unsigned)(code & 15)); }
 
 /* Exact upcast of stored element idx. A bf16 value is the upper 16 bits of a binary32. */
 static double orc_load(const void* base, size_t idx, int dtype) {
@@ -179,20 +192,42 @@ int oracle_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
 }
 
 /*
+ * Element d of kv-head hk in cache row `row` (= block * block_size + offset), before the
+ * per-tensor scale. NVFP4 (the 4-bit KV format with fine-grained E4M3 block scales, page
+ * "From PagedAttention to Prefill-Decode disaggregation", sec. 6.2): the data tensor is
+ * [rows, H_kv, D/2] bytes holding two E2M1 codes each, element d in the low nibble of byte
+ * d/2 when d is even and in the high nibble when d is odd; the scale tensor is
+ * [rows, H_kv, D/16] E4M3 bytes, one per 16 consecutive elements. The element's value is
+ * e2m1(code) * e4m3(scale of its 16-element block).
+ */
+static double orc_kv(const void* cache, const void* block_scales, size_t row, int hk, int d,
+                     int H_kv, int D, int dtype) {
+  const size_t r = row * (size_t)H_kv + (size_t)hk;
+  if (dtype == ORC_NVFP4) {
+    const uint8_t byte = ((const uint8_t*)cache)[r * (size_t)(D / 2) + (size_t)(d / 2)];
+    const unsigned code = (d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15);
+    const uint8_t sc = ((const uint8_t*)block_scales)[r * (size_t)(D / 16) + (size_t)(d / 16)];
+    return orc_e2m1(code) * orc_e4m3(sc);
+  }
+  return orc_load(cache, r * (size_t)D + (size_t)d, dtype);
+}
+
+/*
  * Gather the K and V of kv-head hk of request b into contiguous [L, D] arrays of
- * doubles. Returns 0, or -1 when a block id is out of range.
+ * doubles, each element times its tensor's scale. Returns 0, or -1 when a block id is out
+ * of range.
  */
 static int orc_gather(double* Kc, double* Vc, const void* k_cache, const void* v_cache,
-                      const int32_t* table_row, int L, int hk, int H_kv, int D, int block_size,
-                      int num_blocks, int kv_dtype, double k_scale, double v_scale) {
+                      const void* k_bs, const void* v_bs, const int32_t* table_row, int L,
+                      int hk, int H_kv, int D, int block_size, int num_blocks, int kv_dtype,
+                      double k_scale, double v_scale) {
   for (int t = 0; t < L; ++t) {
     const int32_t block = table_row[t / block_size];
     if (block < 0 || block >= num_blocks) return -1;
     const size_t row = (size_t)block * (size_t)block_size + (size_t)(t % block_size);
-    const size_t base = (row * (size_t)H_kv + (size_t)hk) * (size_t)D;
     for (int d = 0; d < D; ++d) {
-      Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype) * k_scale;
-      Vc[(size_t)t * D + d] = orc_load(v_cache, base + d, kv_dtype) * v_scale;
+      Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype) * k_scale;
+      Vc[(size_t)t * D + d] = orc_kv(v_cache, v_bs, row, hk, d, H_kv, D, kv_dtype) * v_scale;
     }
   }
   return 0;
@@ -210,14 +245,14 @@ static void orc_fill_rows(double* out, int b, int H, int D, double value) {
  * k_scale, a V element its value times v_scale (1 for unquantised caches; for FP8 caches
  * the per-tensor scales of the quantisation). num_threads <= 0 uses the OpenMP default.
  */
-int oracle_paged_decode_attention(double* out, const void* q, const void* k_cache,
-                                  const void* v_cache, const int32_t* block_tables,
-                                  int max_blocks, const int32_t* context_lens, int B, int H,
-                                  int H_kv, int D, int block_size, int num_blocks, float scale,
-                                  int q_dtype, int kv_dtype, float k_scale, float v_scale,
-                                  int num_threads) {
+static int orc_attention(double* out, const void* q, const void* k_cache, const void* v_cache,
+                         const void* k_bs, const void* v_bs, const int32_t* block_tables,
+                         int max_blocks, const int32_t* context_lens, int B, int H, int H_kv,
+                         int D, int block_size, int num_blocks, float scale, int q_dtype,
+                         int kv_dtype, float k_scale, float v_scale, int num_threads) {
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
-      num_blocks <= 0 || max_blocks < 0 || !orc_dtype_ok(q_dtype) || !orc_dtype_ok(kv_dtype))
+      num_blocks <= 0 || max_blocks < 0 || !orc_dtype_ok(q_dtype) ||
+      !(orc_dtype_ok(kv_dtype) || (kv_dtype == ORC_NVFP4 && D % 16 == 0 && k_bs && v_bs)))
     return ORC_ERR_ARG;
   const int group = H / H_kv;
   const double sc = (double)scale;
@@ -248,8 +283,8 @@ int oracle_paged_decode_attention(double* out, const void* q, const void* k_cach
     double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
     const int32_t* row = block_tables + (size_t)b * max_blocks;
-    if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
-                   kv_dtype, (double)k_scale, (double)v_scale) != 0) {
+    if (orc_gather(Kc, Vc, k_cache, v_cache, k_bs, v_bs, row, L, hk, H_kv, D, block_size,
+                   num_blocks, kv_dtype, (double)k_scale, (double)v_scale) != 0) {
       for (int j = 0; j < group; ++j)
         for (int d = 0; d < D; ++d)
           out[((size_t)b * H + (size_t)hk * group + j) * D + d] = NAN;
@@ -285,6 +320,34 @@ int oracle_paged_decode_attention(double* out, const void* q, const void* k_cach
   return status;
 }
 
+int oracle_paged_decode_attention(double* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int max_blocks, const int32_t* context_lens, int B, int H,
+                                  int H_kv, int D, int block_size, int num_blocks, float scale,
+                                  int q_dtype, int kv_dtype, float k_scale, float v_scale,
+                                  int num_threads) {
+  return orc_attention(out, q, k_cache, v_cache, NULL, NULL, block_tables, max_blocks,
+                       context_lens, B, H, H_kv, D, block_size, num_blocks, scale, q_dtype,
+                       kv_dtype, k_scale, v_scale, num_threads);
+}
+
+/*
+ * The same attention over an NVFP4 cache: k_data/v_data are [num_blocks, block_size, H_kv,
+ * D/2] bytes, k_block_scales/v_block_scales [num_blocks, block_size, H_kv, D/16] E4M3 bytes;
+ * a K element means e2m1(code) * e4m3(block scale) * k_scale (see orc_kv).
+ */
+int oracle_paged_decode_attention_nvfp4(double* out, const void* q, const void* k_data,
+                                        const void* v_data, const void* k_block_scales,
+                                        const void* v_block_scales, const int32_t* block_tables,
+                                        int max_blocks, const int32_t* context_lens, int B,
+                                        int H, int H_kv, int D, int block_size, int num_blocks,
+                                        float scale, int q_dtype, float k_scale, float v_scale,
+                                        int num_threads) {
+  return orc_attention(out, q, k_data, v_data, k_block_scales, v_block_scales, block_tables,
+                       max_blocks, context_lens, B, H, H_kv, D, block_size, num_blocks, scale,
+                       q_dtype, ORC_NVFP4, k_scale, v_scale, num_threads);
+}
+
 /*
  * Unnormalised attention of query head h of request b over tokens [t0, t1):
  *   m = max_t s_t,  l = sum_t exp(s_t - m),  o = sum_t exp(s_t - m) V_t.
@@ -303,8 +366,8 @@ int oracle_attention_partial(double* m_out, double* l_out, double* o_out, const 
   double* Kc = (double*)malloc(sizeof(double) * (size_t)L * D);
   double* Vc = (double*)malloc(sizeof(double) * (size_t)L * D);
   const int32_t* row = block_tables + (size_t)b * max_blocks;
-  if (orc_gather(Kc, Vc, k_cache, v_cache, row, L, hk, H_kv, D, block_size, num_blocks,
-                 kv_dtype, 1.0, 1.0) != 0) {
+  if (orc_gather(Kc, Vc, k_cache, v_cache, NULL, NULL, row, L, hk, H_kv, D, block_size,
+                 num_blocks, kv_dtype, 1.0, 1.0) != 0) {
     free(Kc);
     free(Vc);
     return ORC_ERR_DATA;

@@ -59,6 +59,11 @@ def load(path: str | None = None):
                                                       I, I, F, F, I]
         lib.oracle_decode_e4m3.argtypes = [I]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_decode_e2m1.argtypes = [I]
+        lib.oracle_decode_e2m1.restype = ctypes.c_double
+        lib.oracle_paged_decode_attention_nvfp4.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I,
+                                                            I, I, I, F, I, F, F, I]
+        lib.oracle_paged_decode_attention_nvfp4.restype = I
         lib.oracle_paged_decode_attention.restype = I
         lib.oracle_attention_partial.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                                  I, F, I, I]
@@ -116,6 +121,33 @@ def kv_unpack_blocks(packed, k_cache, v_cache, block_table_row, context_len: int
     return lib.oracle_kv_unpack_blocks(_ptr(np.ascontiguousarray(packed)), _ptr(k_cache),
                                        _ptr(v_cache), _ptr(row), int(context_len), H_kv, D, bs,
                                        NB, _dtype_code(k_cache))
+
+
+def decode_e2m1(code: int, lib=None) -> float:
+    """Exact value of one FP4 E2M1 code (0..15)."""
+    return (lib or load()).oracle_decode_e2m1(int(code))
+
+
+def paged_decode_attention_nvfp4(q, k_data, v_data, k_block_scales, v_block_scales,
+                                 block_tables, context_lens, scale: float, k_scale: float = 1.0,
+                                 v_scale: float = 1.0, num_threads: int = 0, lib=None):
+    """fp64 attention over an NVFP4 cache: data [NB, bs, H_kv, D/2] uint8 (two E2M1 codes
+    per byte, even element in the low nibble), block scales [NB, bs, H_kv, D/16] uint8
+    (E4M3). Returns (out[B,H,D] float64, status)."""
+    lib = lib or load()
+    B, H, D = q.shape
+    NB, bs, H_kv, half = k_data.shape
+    assert half * 2 == D and k_data.dtype == np.uint8 and v_data.shape == k_data.shape
+    assert k_block_scales.shape == (NB, bs, H_kv, D // 16) == v_block_scales.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((B, H, D), dtype=np.float64)
+    st = lib.oracle_paged_decode_attention_nvfp4(
+        _ptr(out), _ptr(q), _ptr(k_data), _ptr(v_data), _ptr(k_block_scales),
+        _ptr(v_block_scales), _ptr(bt), bt.shape[1], _ptr(cl), B, H, H_kv, D, bs, NB,
+        ctypes.c_float(scale), _dtype_code(q), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+        int(num_threads))
+    return out, st
 
 
 def decode_e4m3(code: int, lib=None) -> float:

@@ -23,7 +23,9 @@ Facts used:
     unpack touches no row outside the request's tokens;
   - every FP8 E4M3 code decodes to the value torch's own float8_e4m3fn conversion gives,
     and to hand-derived values at the format's landmarks; FP8 attention with per-tensor
-    scales matches the dense brute force run on torch-decoded, scaled values.
+    scales matches the dense brute force run on torch-decoded, scaled values;
+  - every FP4 E2M1 code decodes to the format's table of values; NVFP4 attention matches
+    the dense brute force run on values decoded through that table and torch's E4M3.
 """
 from __future__ import annotations
 
@@ -370,6 +372,60 @@ def pin_fp8_attention_brute_force(lib):
             rows = [(bt[b, t // bs], t % bs) for t in range(L)]
             K = np.stack([dec(kc[r]) for r in rows]) * k_scale
             V = np.stack([dec(vc[r]) for r in rows]) * v_scale
+            ref = brute.dense_decode_attention(stored_to_f64(q[b]), K, V, scale)
+            assert np.abs(out[b] - ref).max() <= 1e-12, (lengths, b)
+
+
+# FP4 E2M1 magnitudes by 3-bit code (sign is the 4th bit), as the format lists them
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def pin_e2m1_decode(lib):
+    for c in range(16):
+        want = (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7]
+        got = orc.decode_e2m1(c, lib=lib)
+        assert got == want and np.signbit(got) == bool(c & 8), (c, got, want)
+
+
+def pin_nvfp4_attention_brute_force(lib):
+    import torch
+
+    rng = np.random.default_rng(24)
+    table = np.array(E2M1_TABLE)
+    for lengths, H, H_kv, D, bs in (([1, 9, 33, 70], 4, 2, 32, 8), ([5, 40], 8, 1, 64, 16)):
+        B = len(lengths)
+        k_scale, v_scale = float(np.float32(0.9)), float(np.float32(1.3))
+        nblk = [(L + bs - 1) // bs for L in lengths]
+        NB = sum(nblk) + 2
+        kd = rng.integers(0, 256, (NB, bs, H_kv, D // 2)).astype(np.uint8)
+        vd = rng.integers(0, 256, (NB, bs, H_kv, D // 2)).astype(np.uint8)
+        # block scales: E4M3 codes of 0.25 .. 0.47 (exponent field 5)
+        ks = rng.integers(0x28, 0x30, (NB, bs, H_kv, D // 16)).astype(np.uint8)
+        vs = rng.integers(0x28, 0x30, (NB, bs, H_kv, D // 16)).astype(np.uint8)
+        perm = rng.permutation(NB).astype(np.int32)
+        bt = np.full((B, max(nblk)), -1, np.int32)
+        off = 0
+        for b, n in enumerate(nblk):
+            bt[b, :n] = perm[off:off + n]
+            off += n
+        q = as_stored(rng.standard_normal((B, H, D)), "bf16")
+        scale = float(np.float32(1.0 / math.sqrt(D)))
+        out, st = orc.paged_decode_attention_nvfp4(q, kd, vd, ks, vs, bt,
+                                                   np.array(lengths, np.int32), scale, k_scale,
+                                                   v_scale, lib=lib)
+        assert st == orc.ORC_OK
+
+        def dequant(data, sc, tensor_scale):
+            lo, hi = data & 15, data >> 4
+            codes = np.stack([lo, hi], axis=-1).reshape(*data.shape[:-1], D)  # even: low
+            vals = np.where(codes & 8, -1.0, 1.0) * table[codes & 7]
+            s = torch.from_numpy(sc).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+            return vals * np.repeat(s, 16, axis=-1) * tensor_scale
+
+        for b, L in enumerate(lengths):
+            rows = [(bt[b, t // bs], t % bs) for t in range(L)]
+            K = np.stack([dequant(kd[r], ks[r], k_scale) for r in rows])
+            V = np.stack([dequant(vd[r], vs[r], v_scale) for r in rows])
             ref = brute.dense_decode_attention(stored_to_f64(q[b]), K, V, scale)
             assert np.abs(out[b] - ref).max() <= 1e-12, (lengths, b)
 

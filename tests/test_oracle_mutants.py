@@ -20,8 +20,8 @@ MUTANTS = [
     ("gqa_strided_grouping",
      [("const int h = hk * group + j;", "const int h = j * H_kv + hk;", None)]),
     ("wrong_row_in_block",
-     [("(size_t)(t % block_size);\n    const size_t base",
-       "(size_t)((t + 1) % block_size);\n    const size_t base", None)]),
+     [("(size_t)(t % block_size);\n    for (int d = 0; d < D; ++d) {\n      Kc",
+       "(size_t)((t + 1) % block_size);\n    for (int d = 0; d < D; ++d) {\n      Kc", None)]),
     ("scale_dropped", [("s[t] = sc * dot;", "s[t] = dot;", None)]),
     ("no_max_subtraction",
      [("den += exp(s[t] - mx);", "den += exp(s[t]);", None),
@@ -57,9 +57,17 @@ MUTANTS = [
     ("combine_forgets_weights", [("Lsum += l[j] * exp(m[j] - M);", "Lsum += l[j];", None)]),
     ("e4m3_wrong_bias", [("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)", None)]),
     ("e4m3_wrong_subnormal", [("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)", None)]),
+    ("e2m1_wrong_bias", [("ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)", None)]),
+    ("nvfp4_nibbles_swapped",
+     [("(d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15)",
+       "(d & 1) ? (unsigned)(byte & 15) : (unsigned)(byte >> 4)", None)]),
+    ("nvfp4_wrong_block_index",
+     [("r * (size_t)(D / 16) + (size_t)(d / 16)", "r * (size_t)(D / 16) + (size_t)(d / 32)", None)]),
+    ("nvfp4_block_scale_dropped",
+     [("return orc_e2m1(code) * orc_e4m3(sc);", "(void)sc; return orc_e2m1(code);", None)]),
     ("kv_scale_dropped",
-     [("Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype) * k_scale;",
-       "Kc[(size_t)t * D + d] = orc_load(k_cache, base + d, kv_dtype);", None)]),
+     [("Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype) * k_scale;",
+       "Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype);", None)]),
 ]
 
 
