@@ -60,9 +60,9 @@ def step_bytes(s, pack_reqs) -> dict:
     L = s.context_lens_np.astype(np.int64)
     bs = w.block_size
     nblk = (L + bs - 1) // bs
-    kv_tok = 2 * w.H_kv * w.D * e_kv
+    kv_tok = int(round(2 * w.H_kv * w.D * e_kv))  # NVFP4: codes and block scales
     attn = int(L.sum()) * kv_tok + 2 * s.B * w.H * w.D * e + int(nblk.sum()) * 4 + s.B * 4
-    append = 2 * s.B * 2 * w.H_kv * w.D * e_kv + s.B * 4
+    append = 2 * s.B * kv_tok + s.B * 4
     pl = np.array([int(L[r]) for r in pack_reqs], np.int64)
     pack = int(pl.sum()) * kv_tok * 2 + int(((pl + bs - 1) // bs).sum()) * 4
     return {"attention": attn, "append": append, "pack": pack,
@@ -183,6 +183,12 @@ class L2Flush:
 def attention(s, out, sm_cap, workspace, error_word=None, stream=None):
     """One attention call through the C ABI (the FP8 entry point for FP8 caches)."""
     import paged_decode_attention_02_gb300 as pda
+    if s.w.kv == "nvfp4":
+        return pda.paged_decode_attention_nvfp4(out, s.q, s.k_cache, s.v_cache, s.k_bscales,
+                                                s.v_bscales, s.block_tables, s.context_lens,
+                                                s.max_context_len, s.scale, s.k_scale,
+                                                s.v_scale, sm_cap=sm_cap, workspace=workspace,
+                                                error_word=error_word, stream=stream)
     if s.w.kv == "fp8":
         return pda.paged_decode_attention_fp8(out, s.q, s.k_cache, s.v_cache, s.block_tables,
                                               s.context_lens, s.max_context_len, s.scale,
@@ -491,7 +497,7 @@ def sweep_workloads(args, dev, flush, peak):
     sms = pda.device_sm_count()
     stream = torch.cuda.current_stream(dev)
     for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
-                 "gqa_skew_b256_fp8"):
+                 "gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4", "gqa_skew_b256_nvfp4"):
         if name == args.config:
             continue
         w = wl.get(name)
@@ -501,8 +507,10 @@ def sweep_workloads(args, dev, flush, peak):
         res_w = {}
         for cap in caps:
             out = torch.empty_like(s.q)
-            wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype,
-                                      cap, dev)
+            wsp = (pda.binding.nvfp4_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, cap, dev)
+                   if w.kv == "nvfp4" else
+                   pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype,
+                                       cap, dev))
             for _ in range(3):
                 flush()
                 attention(s, out, cap, wsp)

@@ -54,8 +54,10 @@ typedef enum {
 
 /* Element types. PDA_FP8_E4M3 (the OCP 8-bit format without infinities) is a KV-cache type
  * only: append, pack and unpack copy its bytes, and pda_paged_decode_attention_fp8 reads it
- * with per-tensor scales. */
-typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2 } pda_dtype;
+ * with per-tensor scales. PDA_NVFP4 names the 4-bit cache read by
+ * pda_paged_decode_attention_nvfp4 (and sizes its workspace); its data and scale tensors are
+ * plain byte arrays that append, pack and unpack copy as 1-byte elements (see that call). */
+typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2, PDA_NVFP4 = 3 } pda_dtype;
 
 /* Bits OR-ed into *error_word by the kernels. */
 #define PDA_DEVERR_CONTEXT_LEN 0x1 /* context_lens[b] < 0, > max_context_len or > table capacity */
@@ -185,6 +187,44 @@ pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* 
                                           pda_dtype out_dtype, int sm_cap, void* workspace,
                                           size_t workspace_bytes, int32_t* error_word,
                                           cudaStream_t stream);
+
+/*
+ * pda_paged_decode_attention_nvfp4 -- pda_paged_decode_attention over an NVFP4 KV cache.
+ *
+ * The 4-bit KV format with fine-grained block scaling in E4M3 (page "From PagedAttention to
+ * Prefill-Decode disaggregation", sec. 6.2: NVFP4 KV stores 4-bit values with fine-grained
+ * block scales and E4M3 scale factors). Element d of the K row of (token row r, kv-head h)
+ * means  e2m1(code) * e4m3(block scale) * k_scale,  with
+ *   code        = nibble d % 2 (0: low, 1: high) of k_data[r][h][d / 2],
+ *   block scale = k_block_scales[r][h][d / 16]   (one per 16 consecutive elements),
+ * and the same for V. E2M1 is the 4-bit float with 2 exponent bits (bias 1) and 1 mantissa
+ * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Values are widened exactly to fp32 in
+ * registers (the pages describe a dequantisation to FP8 before attention; fp32 holds every
+ * product e2m1 * e4m3 exactly, so nothing is rounded before the softmax arithmetic).
+ *
+ *  k_data, v_data   [num_blocks, block_size, H_kv, D / 2] bytes.
+ *  k_block_scales, v_block_scales [num_blocks, block_size, H_kv, D / 16] E4M3 bytes,
+ *                   16-byte aligned.
+ *  q                [B, H, D] in q_dtype, which must be PDA_BF16.
+ *  k_scale, v_scale finite per-tensor scales.
+ *  Every other argument, the workspace (pda_attention_workspace_size with PDA_NVFP4), the
+ *  supported sizes and the errors are those of pda_paged_decode_attention.
+ *  Append, pack and unpack: both tensors are token-major byte caches, so pda_kv_append,
+ *  pda_kv_pack_blocks[_batched] and pda_kv_unpack_blocks[_batched] move them with kv_dtype
+ *  PDA_FP8_E4M3 (any 1-byte type) and D / 2 (data) or D / 16 (scales) as the row length,
+ *  one call per tensor pair; each needs H_kv * row length to be a multiple of 16 bytes.
+ */
+pda_status pda_paged_decode_attention_nvfp4(void* out, const void* q, const void* k_data,
+                                            const void* v_data, const void* k_block_scales,
+                                            const void* v_block_scales,
+                                            const int32_t* block_tables, int max_blocks_per_seq,
+                                            const int32_t* context_lens, int max_context_len,
+                                            int B, int H, int H_kv, int D, int block_size,
+                                            int num_blocks, float scale, float k_scale,
+                                            float v_scale, pda_dtype q_dtype,
+                                            pda_dtype out_dtype, int sm_cap, void* workspace,
+                                            size_t workspace_bytes, int32_t* error_word,
+                                            cudaStream_t stream);
 
 /*
  * pda_paged_decode_attention_noalloc -- pda_paged_decode_attention without a workspace

@@ -6,10 +6,11 @@ The computation lives in ``libpda.so`` (CUDA kernels behind the C ABI of ``inclu
 from .binding import (PdaDeviceError, PdaError, alloc_workspace, check_error, attention_workspace_size, device_sm_count,
                       kv_append, kv_pack_blocks, kv_pack_blocks_batched, kv_unpack_blocks,
                       kv_unpack_blocks_batched, paged_decode_attention,
-                      paged_decode_attention_fp8,
+                      paged_decode_attention_fp8, paged_decode_attention_nvfp4,
                       paged_decode_attention_noalloc, status_string)
 
 __all__ = ["PdaDeviceError", "PdaError", "alloc_workspace", "check_error", "attention_workspace_size", "device_sm_count",
            "kv_append", "kv_pack_blocks", "kv_pack_blocks_batched", "kv_unpack_blocks",
-           "kv_unpack_blocks_batched", "paged_decode_attention", "paged_decode_attention_fp8", "paged_decode_attention_noalloc",
+           "kv_unpack_blocks_batched", "paged_decode_attention", "paged_decode_attention_fp8",
+           "paged_decode_attention_nvfp4", "paged_decode_attention_noalloc",
            "status_string"]

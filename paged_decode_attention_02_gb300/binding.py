@@ -17,7 +17,7 @@ from . import build_lib
 
 (PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE,
  PDA_ERR_TOO_LARGE) = range(6)
-PDA_F32, PDA_BF16, PDA_FP8_E4M3 = 0, 1, 2
+PDA_F32, PDA_BF16, PDA_FP8_E4M3, PDA_NVFP4 = 0, 1, 2, 3
 PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PDA_PACK_MAX_BATCH = 64
 PDA_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -27,6 +27,7 @@ EXPORTED = [
     "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
     "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
     "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched", "pda_paged_decode_attention_fp8",
+    "pda_paged_decode_attention_nvfp4",
 ]
 
 _lock = threading.Lock()
@@ -69,6 +70,9 @@ def load():
         lib.pda_paged_decode_attention_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I,
                                                        F, F, F, I, I, I, P, SZ, P, P]
         lib.pda_paged_decode_attention_fp8.restype = I
+        lib.pda_paged_decode_attention_nvfp4.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I,
+                                                         I, I, I, F, F, F, I, I, I, P, SZ, P, P]
+        lib.pda_paged_decode_attention_nvfp4.restype = I
         lib.pda_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I,
                                                            I, I, F, I, I, I, I, P, P]
         lib.pda_paged_decode_attention_noalloc.restype = I
@@ -218,6 +222,41 @@ def paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables, context_l
         workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
         "pda_paged_decode_attention_fp8")
     return out
+
+
+def paged_decode_attention_nvfp4(out, q, k_data, v_data, k_block_scales, v_block_scales,
+                                 block_tables, context_lens, max_context_len: int, scale: float,
+                                 k_scale: float, v_scale: float, sm_cap: int = 0, workspace=None,
+                                 error_word=None, stream=None):
+    """Attention over an NVFP4 cache: data [NB, bs, H_kv, D/2] uint8 (two E2M1 codes per
+    byte, even element low), block scales [NB, bs, H_kv, D/16] uint8 (E4M3)."""
+    B, H, D = q.shape
+    NB, bs, H_kv, half = k_data.shape
+    assert 2 * half == D and v_data.shape == k_data.shape and out.shape == q.shape
+    assert tuple(k_block_scales.shape) == (NB, bs, H_kv, D // 16)
+    assert v_block_scales.shape == k_block_scales.shape
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(load().pda_attention_workspace_size(B, H, H_kv, D, bs, PDA_NVFP4, sm_cap,
+                                                   ctypes.byref(n)), "workspace size")
+        workspace = torch.empty(max(n.value, 256), dtype=torch.uint8, device=q.device)
+    _check(load().pda_paged_decode_attention_nvfp4(
+        _ptr(out), _ptr(q), _ptr(k_data), _ptr(v_data), _ptr(k_block_scales),
+        _ptr(v_block_scales), _ptr(block_tables), max_blocks, _ptr(context_lens),
+        int(max_context_len), B, H, H_kv, D, bs, NB, float(scale), float(k_scale),
+        float(v_scale), _dtype(q), _dtype(out), int(sm_cap), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(error_word), _stream(stream)),
+        "pda_paged_decode_attention_nvfp4")
+    return out
+
+
+def nvfp4_workspace(B, H, H_kv, D, block_size=16, sm_cap=0, device=None) -> torch.Tensor:
+    n = ctypes.c_size_t(0)
+    _check(load().pda_attention_workspace_size(B, H, H_kv, D, block_size, PDA_NVFP4, sm_cap,
+                                               ctypes.byref(n)), "workspace size")
+    return torch.empty(max(n.value, 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,

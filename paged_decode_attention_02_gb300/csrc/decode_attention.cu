@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <mutex>
 #include <utility>
@@ -70,6 +71,8 @@ struct AttnParams {
   unsigned long long call;        // this call's number (48 bits)
   int32_t* error_word;
   float v_scale;                  // value of a stored V element = code * v_scale (1 if plain)
+  const uint8_t* k_bscales;       // NVFP4: [rows, H_kv, D/16] E4M3 block scales (else null)
+  const uint8_t* v_bscales;
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
   int out_bf16;
   float scale_log2;
@@ -123,12 +126,17 @@ struct Geometry {
   static constexpr int LPH = N >= LPR ? LPR / G : LPR;  // lanes of a row group per head
   // Scores of two token slots share one packed fp32x2 FMA when q fits twice in registers.
   static constexpr bool PAIR_QK = G * VEC <= 32 && TPL % 2 == 0;
-  static constexpr uint32_t TILE_BYTES = kBS * D * sizeof(KV);
+  // NVFP4: every row of a tile comes with one E4M3 scale per 16 elements
+  static constexpr bool SCALED = std::is_same<KV, nvfp4>::value;
+  static constexpr int ROW_SCALES = D / 16;  // scale bytes per row (NVFP4)
+  static constexpr uint32_t TILE_BYTES = kBS * D * E::kBits / 8;
+  static constexpr uint32_t SCALE_BYTES = SCALED ? kBS * ROW_SCALES : 0;  // per K or V tile
   static constexpr uint32_t Q_BYTES = G * D * sizeof(QT);
   static_assert(32 % LPR == 0 && kBS % RPW == 0, "row geometry");
   static_assert(LPR >= G, "one head per lane after the reduce-scatter");
   static_assert(VEC % 2 == 0, "packed fp32x2 accumulation");
   static_assert(TILE_BYTES % 128 == 0 && Q_BYTES % 16 == 0, "smem alignment");
+  static_assert(!SCALED || (VEC <= 16 && 16 % VEC == 0), "a lane's dims share one scale");
 };
 
 // Per-warp online-softmax state and tile arithmetic.
@@ -145,8 +153,12 @@ struct WarpAttn {
   static constexpr int VEC = Geo::VEC, LPR = Geo::LPR, RPW = Geo::RPW, TPL = Geo::TPL;
   static constexpr int N = Geo::N, C = Geo::C, DUP = Geo::DUP, LPH = Geo::LPH;
   static constexpr bool PAIR_QK = Geo::PAIR_QK;
+  static constexpr bool SCALED = Geo::SCALED;
+  static constexpr int ROW_SCALES = Geo::ROW_SCALES;
 
   int lane, rw, cl, idx0;
+  int sblk;                      // NVFP4: index of this lane's 16-element block in a row
+  int srow[SCALED ? TPL : 1];    // NVFP4: scale offset of the K row behind local slot il
   int hp;             // local head jl holds real head jl ^ hp
   int krow[TPL];      // element offset of the K row behind local slot il (real slot il ^ tp)
   float2 q2[PAIR_QK ? G : 1][PAIR_QK ? VEC : 1];  // q (scaled), duplicated, local head order
@@ -164,6 +176,11 @@ struct WarpAttn {
     const int tp = idx0 % TPL;
 #pragma unroll
     for (int il = 0; il < TPL; ++il) krow[il] = (rw + RPW * (il ^ tp)) * D + cl * VEC;
+    sblk = (cl * VEC) / 16;
+    if constexpr (SCALED) {
+#pragma unroll
+      for (int il = 0; il < TPL; ++il) srow[il] = (rw + RPW * (il ^ tp)) * ROW_SCALES + sblk;
+    }
   }
 
   __device__ __forceinline__ void reset(const QT* q_smem, float scale_log2) {
@@ -188,22 +205,28 @@ struct WarpAttn {
     l_own = 0.f;
   }
 
+  // ksc/vsc: the tile's NVFP4 block scales ([16 rows][D/16] E4M3 bytes), unused otherwise.
   template <bool kPartial>
-  __device__ __forceinline__ void tile(const KV* ks, const KV* vs, int n_valid) {
+  __device__ __forceinline__ void tile(const KV* ks, const KV* vs, const uint8_t* ksc,
+                                       const uint8_t* vsc, int n_valid) {
     // ---- scores: part[jl * TPL + il] = q(real head jl ^ hp) . K(real slot il ^ tp)
     float part[N];
     if constexpr (PAIR_QK) {
 #pragma unroll
       for (int m = 0; m < TPL / 2; ++m) {
         float k0[VEC], k1[VEC];
-        E::load(ks + krow[2 * m], k0);
-        E::load(ks + krow[2 * m + 1], k1);
+        E::load(elem_ptr<KV>(ks, krow[2 * m]), k0);
+        E::load(elem_ptr<KV>(ks, krow[2 * m + 1]), k1);
+        float2 sk = make_float2(1.f, 1.f);
+        if constexpr (SCALED)
+          sk = make_float2(e4m3_to_f32(ksc[srow[2 * m]]), e4m3_to_f32(ksc[srow[2 * m + 1]]));
 #pragma unroll
         for (int jl = 0; jl < G; ++jl) {
           float2 acc = __fmul2_rn(q2[jl][0], make_float2(k0[0], k1[0]));
 #pragma unroll
           for (int e = 1; e < VEC; ++e)
             acc = __ffma2_rn(q2[jl][e], make_float2(k0[e], k1[e]), acc);
+          if constexpr (SCALED) acc = __fmul2_rn(acc, sk);
           part[jl * TPL + 2 * m] = acc.x;
           part[jl * TPL + 2 * m + 1] = acc.y;
         }
@@ -212,13 +235,15 @@ struct WarpAttn {
 #pragma unroll
       for (int il = 0; il < TPL; ++il) {
         float k[VEC];
-        E::load(ks + krow[il], k);
+        E::load(elem_ptr<KV>(ks, krow[il]), k);
+        float sk = 1.f;
+        if constexpr (SCALED) sk = e4m3_to_f32(ksc[srow[il]]);
 #pragma unroll
         for (int jl = 0; jl < G; ++jl) {
           float acc = qs[jl][0] * k[0];
 #pragma unroll
           for (int e = 1; e < VEC; ++e) acc = fmaf(qs[jl][e], k[e], acc);
-          part[jl * TPL + il] = acc;
+          part[jl * TPL + il] = SCALED ? acc * sk : acc;
         }
       }
     }
@@ -265,16 +290,20 @@ struct WarpAttn {
     for (int i = 0; i < TPL; ++i) {
       const int t = rw + RPW * i;
       float v[VEC];
-      E::load(vs + t * D + cl * VEC, v);
+      E::load(elem_ptr<KV>(vs, t * D + cl * VEC), v);
+      float sv = 1.f;  // NVFP4: this lane's block scale of row t, folded into p
+      if constexpr (SCALED) sv = e4m3_to_f32(vsc[t * ROW_SCALES + sblk]);
       if (kPartial && t >= n_valid) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[e] = 0.f;
+        sv = 0.f;
       }
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const int idx = j * TPL + i;
         const int src = rw * LPR + (idx / C) * DUP;
-        const float p = __shfl_sync(kFullMask, part[idx % C], src);
+        float p = __shfl_sync(kFullMask, part[idx % C], src);
+        if constexpr (SCALED) p *= sv;
         const float2 p2 = make_float2(p, p);
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e)
@@ -509,7 +538,9 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
   }
   // barrier init (one lane per warp, its own stages)
   if (lane == 0) {
-    for (int s = 0; s < p.stages; ++s) mbar_init(&s_bar[warp * p.stages + s], 1);
+    // one arrive carries the TMA byte count; NVFP4 adds one per lane for the scale copies
+    for (int s = 0; s < p.stages; ++s)
+      mbar_init(&s_bar[warp * p.stages + s], Geo::SCALED ? 33 : 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -546,8 +577,16 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
   auto v_buf = [&](int s) {
     return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + Geo::TILE_BYTES);
   };
+  auto ks_buf = [&](int s) {  // NVFP4 block scales of the K tile, [16][D/16]
+    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
+  };
+  auto vs_buf = [&](int s) {
+    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES +
+                                      Geo::SCALE_BYTES);
+  };
   auto q_buf = [&](int s) {
-    return reinterpret_cast<QT*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
+    return reinterpret_cast<QT*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES +
+                                 2 * Geo::SCALE_BYTES);
   };
 
   // (request, kv-head, block) of tile y
@@ -605,6 +644,21 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
   enter(t_begin, 0);
   auto issue = [&](int x, int s) {
     if (x >= g_base + 32) enter(g_base + 32, g_buf ^ 1);
+    if constexpr (Geo::SCALED) {
+      // lanes 0-15 copy the 16 K scale rows of the tile, lanes 16-31 the V rows; each copy
+      // arrives on the stage barrier when it lands
+      const int src_lane = x - g_base;
+      int pid = __shfl_sync(kFullMask, cur_pid, src_lane);
+      const int h = __shfl_sync(kFullMask, cur_h, src_lane);
+      if (pid < 0 || pid >= p.num_blocks) pid = 0;  // flagged below; read a valid block
+      const int r = lane & 15;
+      const bool is_v = lane >= 16;
+      const uint8_t* src = (is_v ? p.v_bscales : p.k_bscales) +
+                           ((static_cast<size_t>(pid) * kBS + r) * H_kv + h) * Geo::ROW_SCALES;
+      uint8_t* dst = (is_v ? vs_buf(s) : ks_buf(s)) + r * Geo::ROW_SCALES;
+      cp_async_n<Geo::ROW_SCALES>(dst, src);
+      cp_async_mbar_arrive_noinc(&my_bar[s]);
+    }
     if (lane == x - g_base) {
       const bool bad = cur_pid < 0 || cur_pid >= p.num_blocks;
       const bool need_q = (cur_blk == 0) || (x == t_begin);
@@ -658,9 +712,11 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
     }
     seg_bad |= (info & 0x100) != 0;
     if (n_valid == kBS)
-      st.template tile<false>(k_buf(stage), v_buf(stage), n_valid);
+      st.template tile<false>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
+                              n_valid);
     else
-      st.template tile<true>(k_buf(stage), v_buf(stage), n_valid);
+      st.template tile<true>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
+                             n_valid);
 
     // hand the stage back to the TMA engine
     __syncwarp();
@@ -758,13 +814,17 @@ struct LaunchPlan {
   size_t ws_arrive, ws_ml, ws_o, ws_total;  // byte offsets / total
 };
 
-// q is bf16 beside an FP8 cache, otherwise of the cache's own type.
-size_t q_bytes_for(pda_dtype kv) { return kv == PDA_FP8_E4M3 ? 2u : dtype_bytes(kv); }
+// q is bf16 beside a quantised cache, otherwise of the cache's own type.
+size_t q_bytes_for(pda_dtype kv) {
+  return (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4) ? 2u : dtype_bytes(kv);
+}
 
+// One pipeline stage: the K and V tiles, (NVFP4) their block scales, the q rows.
 uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
-  const uint32_t tile = kBS * D * static_cast<uint32_t>(dtype_bytes(kv));
-  return 2 * tile +
-         static_cast<uint32_t>(round_up(static_cast<size_t>(G) * D * q_bytes_for(kv), 128));
+  const size_t tile = kv == PDA_NVFP4 ? kBS * D / 2 : kBS * D * dtype_bytes(kv);
+  const size_t scales = kv == PDA_NVFP4 ? 2 * kBS * D / 16 : 0;
+  const size_t q = static_cast<size_t>(G) * D * q_bytes_for(kv);
+  return static_cast<uint32_t>(round_up(2 * tile + scales + q, 128));
 }
 
 bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
@@ -823,6 +883,9 @@ KernelFn pick_kernel(pda_dtype kv, int D, int G) {
   } else if (kv == PDA_FP8_E4M3) {
     if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128>(G);
     if (D == 64) return pick_g<fp8e4m3, __nv_bfloat16, 64>(G);
+  } else if (kv == PDA_NVFP4) {
+    if (D == 128) return pick_g<nvfp4, __nv_bfloat16, 128>(G);
+    if (D == 64) return pick_g<nvfp4, __nv_bfloat16, 64>(G);
   } else {
     if (D == 128) return pick_g<float, float, 128>(G);
     if (D == 64) return pick_g<float, float, 64>(G);
@@ -896,7 +959,7 @@ extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D
                                                    pda_dtype kv_dtype, int sm_cap,
                                                    size_t* bytes) {
   if (bytes == nullptr || B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 ||
-      block_size <= 0 || sm_cap < 0 || !dtype_ok(kv_dtype))
+      block_size <= 0 || sm_cap < 0 || !(dtype_ok(kv_dtype) || kv_dtype == PDA_NVFP4))
     return PDA_ERR_INVALID_ARG;
   if (block_size != kBS || (D != 64 && D != 128) || !supported_g(H / H_kv) || B > kMaxBatch)
     return PDA_ERR_UNSUPPORTED;
@@ -915,6 +978,7 @@ namespace {
 // The attention launch behind every public entry point. kv_dtype selects the cache format;
 // k_scale and v_scale are the values of one stored unit of K and V (1 for plain caches).
 pda_status launch_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const void* k_bscales, const void* v_bscales,
                             const int32_t* block_tables, int max_blocks_per_seq,
                             const int32_t* context_lens, int max_context_len, int B, int H,
                             int H_kv, int D, int block_size, int num_blocks, float scale,
@@ -925,7 +989,8 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   // ---- host-side validation, before any CUDA call
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || sm_cap < 0 ||
-      !float_dtype_ok(q_dtype) || !dtype_ok(kv_dtype) || !float_dtype_ok(out_dtype) ||
+      !float_dtype_ok(q_dtype) || !(dtype_ok(kv_dtype) || kv_dtype == PDA_NVFP4) ||
+      !float_dtype_ok(out_dtype) ||
       !isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale))
     return PDA_ERR_INVALID_ARG;
   if (B == 0) return PDA_OK;
@@ -934,8 +999,12 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
     return PDA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PDA_ERR_INVALID_ARG;
+  if (kv_dtype == PDA_NVFP4 && (k_bscales == nullptr || v_bscales == nullptr ||
+                                !aligned16(k_bscales) || !aligned16(v_bscales)))
+    return PDA_ERR_INVALID_ARG;
   const int G = H / H_kv;
-  const bool q_ok = kv_dtype == PDA_FP8_E4M3 ? q_dtype == PDA_BF16 : q_dtype == kv_dtype;
+  const bool quantised = kv_dtype == PDA_FP8_E4M3 || kv_dtype == PDA_NVFP4;
+  const bool q_ok = quantised ? q_dtype == PDA_BF16 : q_dtype == kv_dtype;
   if (block_size != kBS || (D != 64 && D != 128) || !supported_g(G) || !q_ok ||
       B > kMaxBatch)
     return PDA_ERR_UNSUPPORTED;
@@ -957,10 +1026,13 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
   if (st != PDA_OK) return st;
 
+  // the TMA sees an NVFP4 row as D/2 bytes
+  const int row_elems = kv_dtype == PDA_NVFP4 ? D / 2 : D;
+  const pda_dtype map_type = kv_dtype == PDA_NVFP4 ? PDA_FP8_E4M3 : kv_dtype;
   CUtensorMap tmK, tmV;
-  st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, row_elems, map_type);
   if (st != PDA_OK) return st;
-  st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, D, kv_dtype);
+  st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, row_elems, map_type);
   if (st != PDA_OK) return st;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -975,6 +1047,8 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
   ap.error_word = error_word;
   ap.v_scale = v_scale;
+  ap.k_bscales = static_cast<const uint8_t*>(k_bscales);
+  ap.v_bscales = static_cast<const uint8_t*>(v_bscales);
   ap.B = B;
   ap.H = H;
   ap.H_kv = H_kv;
@@ -1004,10 +1078,10 @@ extern "C" pda_status pda_paged_decode_attention(
     float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
     void* workspace, size_t workspace_bytes, int32_t* error_word, cudaStream_t stream) {
   if (kv_dtype == PDA_FP8_E4M3) return PDA_ERR_UNSUPPORTED;  // needs its scales: _fp8 entry
-  return launch_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                          context_lens, max_context_len, B, H, H_kv, D, block_size, num_blocks,
-                          scale, 1.f, 1.f, q_dtype, kv_dtype, out_dtype, sm_cap, workspace,
-                          workspace_bytes, error_word, stream);
+  return launch_attention(out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, B, H, H_kv, D,
+                          block_size, num_blocks, scale, 1.f, 1.f, q_dtype, kv_dtype, out_dtype,
+                          sm_cap, workspace, workspace_bytes, error_word, stream);
 }
 
 extern "C" pda_status pda_paged_decode_attention_fp8(
@@ -1017,10 +1091,25 @@ extern "C" pda_status pda_paged_decode_attention_fp8(
     float scale, float k_scale, float v_scale, pda_dtype q_dtype, pda_dtype out_dtype,
     int sm_cap, void* workspace, size_t workspace_bytes, int32_t* error_word,
     cudaStream_t stream) {
-  return launch_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                          context_lens, max_context_len, B, H, H_kv, D, block_size, num_blocks,
-                          scale, k_scale, v_scale, q_dtype, PDA_FP8_E4M3, out_dtype, sm_cap,
-                          workspace, workspace_bytes, error_word, stream);
+  return launch_attention(out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, B, H, H_kv, D,
+                          block_size, num_blocks, scale, k_scale, v_scale, q_dtype,
+                          PDA_FP8_E4M3, out_dtype, sm_cap, workspace, workspace_bytes,
+                          error_word, stream);
+}
+
+extern "C" pda_status pda_paged_decode_attention_nvfp4(
+    void* out, const void* q, const void* k_data, const void* v_data,
+    const void* k_block_scales, const void* v_block_scales, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int B, int H,
+    int H_kv, int D, int block_size, int num_blocks, float scale, float k_scale, float v_scale,
+    pda_dtype q_dtype, pda_dtype out_dtype, int sm_cap, void* workspace,
+    size_t workspace_bytes, int32_t* error_word, cudaStream_t stream) {
+  return launch_attention(out, q, k_data, v_data, k_block_scales, v_block_scales,
+                          block_tables, max_blocks_per_seq, context_lens, max_context_len, B, H,
+                          H_kv, D, block_size, num_blocks, scale, k_scale, v_scale, q_dtype,
+                          PDA_NVFP4, out_dtype, sm_cap, workspace, workspace_bytes, error_word,
+                          stream);
 }
 
 // ------------------------------------------------------------------ no-allocation variant

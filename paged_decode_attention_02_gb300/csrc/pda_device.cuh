@@ -113,6 +113,20 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
                "l"(reinterpret_cast<uint64_t>(src))
                : "memory");
 }
+// cp.async of `bytes` (4, 8 or 16, both addresses aligned to it) global -> shared.
+template <int bytes>
+__device__ __forceinline__ void cp_async_n(void* dst, const void* src) {
+  static_assert(bytes == 4 || bytes == 8 || bytes == 16, "cp.async sizes");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "n"(bytes)
+               : "memory");
+}
+// When all of this thread's earlier cp.async copies have landed, performs one arrive on
+// `bar` (counted in the barrier's initial arrival count: no pending increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -141,6 +155,11 @@ __device__ __forceinline__ void atomic_or_error(int32_t* error_word, int32_t bit
 struct fp8e4m3 {
   uint8_t bits;
 };
+// Two FP4 E2M1 codes per byte (even element in the low nibble); the values of a row come
+// with one E4M3 scale per 16 elements, held in a separate tensor.
+struct nvfp4 {
+  uint8_t bits;
+};
 
 template <typename T>
 struct Elem;
@@ -148,6 +167,7 @@ struct Elem;
 // Each lane moves kVec elements per access; load() widens them exactly to fp32.
 template <>
 struct Elem<float> {
+  static constexpr int kBits = 32;
   static constexpr int kBytes = 4;
   static constexpr int kVec = 4;  // one 16-byte access
   static __device__ __forceinline__ void load(const void* p, float* out) {
@@ -161,6 +181,7 @@ struct Elem<float> {
 
 template <>
 struct Elem<__nv_bfloat16> {
+  static constexpr int kBits = 16;
   static constexpr int kBytes = 2;
   static constexpr int kVec = 8;  // one 16-byte access
   static __device__ __forceinline__ void load(const void* p, float* out) {
@@ -195,6 +216,7 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* out) {
 
 template <>
 struct Elem<fp8e4m3> {
+  static constexpr int kBits = 8;
   static constexpr int kBytes = 1;
   static constexpr int kVec = 8;  // one 8-byte access (keeps the bf16 lane geometry)
   static __device__ __forceinline__ void load(const void* p, float* out) {
@@ -203,6 +225,48 @@ struct Elem<fp8e4m3> {
     e4m3x4_to_f32(v.y, out + 4);
   }
 };
+
+// One E4M3 code (in the low byte of w) widened exactly to fp32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t w) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(h)
+      : "r"(w & 0xffu));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu)));
+}
+
+template <>
+struct Elem<nvfp4> {
+  static constexpr int kBits = 4;
+  static constexpr int kVec = 8;  // one 4-byte access: 8 codes of one 16-element block
+  // The raw E2M1 values (without the block scale), widened exactly to fp32.
+  static __device__ __forceinline__ void load(const void* p, float* out) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+      out[2 * i] = f.x;
+      out[2 * i + 1] = f.y;
+    }
+  }
+};
+
+// Address of element `off` of a row of T that starts at `base`.
+template <typename T>
+__device__ __forceinline__ const void* elem_ptr(const void* base, int off) {
+  return reinterpret_cast<const unsigned char*>(base) + (off * Elem<T>::kBits) / 8;
+}
 
 // Loads n elements of type T (n a multiple of Elem<T>::kVec) widened to fp32.
 template <typename T, int n>

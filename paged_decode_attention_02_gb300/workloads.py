@@ -23,6 +23,8 @@ Recipe (one per named workload):
   - FP8 workloads store E4M3 codes of value / scale (per-tensor scales, K and V apart;
     torch's float8_e4m3fn rounding), drawn with the seeds of their bf16 twin so the
     lengths and tables are the same;
+  - NVFP4 workloads store random E2M1 code bytes and random E4M3 block scales in
+    [0.25, 0.47) (per-tensor scales 0.9 for K, 1.3 for V), also on their twin's seeds;
   - context lengths count the tokens after this step's append, so the appended token is
     the last position each request attends to; ``slot_mapping[b]`` points at it.
 """
@@ -52,7 +54,7 @@ class Workload:
     pack_top: int = 0  # number of longest requests whose KV is packed each step
     sm_caps_pct: tuple = field(default_factory=tuple)  # SM-fraction sweep, % of SMs
     description: str = ""
-    kv: str = ""  # "" : the cache holds `dtype`; "fp8": FP8 E4M3 codes with per-tensor scales
+    kv: str = ""  # "": the cache holds `dtype`; "fp8": FP8 E4M3 codes; "nvfp4": E2M1 + scales
     k_scale: float = 1.0  # value of one K code unit (FP8 caches)
     v_scale: float = 1.0
     seed_of: int = 0  # draw with another workload's seeds (same lengths and tables)
@@ -71,12 +73,15 @@ class Workload:
         return 4 if self.dtype == "f32" else 2
 
     @property
-    def kv_elem_bytes(self) -> int:
+    def kv_elem_bytes(self) -> float:
+        """Bytes of one stored K (or V) element, block scales included for NVFP4."""
+        if self.kv == "nvfp4":
+            return 0.5 + 1 / 16
         return 1 if self.kv == "fp8" else self.elem_bytes
 
     @property
     def kv_torch_dtype(self):
-        return torch.uint8 if self.kv == "fp8" else self.torch_dtype
+        return torch.uint8 if self.kv in ("fp8", "nvfp4") else self.torch_dtype
 
 
 WORKLOADS = {
@@ -107,6 +112,14 @@ WORKLOADS = {
                  dtype="bf16", lengths="uniform:128,4096", pool="scaled:1.25", kv="fp8",
                  k_scale=0.03, v_scale=0.05, seed_of=3,
                  description="llama2_13b_b80 with an FP8 E4M3 KV cache (per-tensor scales)"),
+        Workload("gqa_skew_b256_nvfp4", 8, B=256, H=32, H_kv=8, D=128, block_size=16,
+                 dtype="bf16", lengths="loguniform:16,32768", pool="scaled:1.25", pack_top=8,
+                 kv="nvfp4", k_scale=0.9, v_scale=1.3, seed_of=4,
+                 description="gqa_skew_b256 with an NVFP4 KV cache"),
+        Workload("llama2_13b_b80_nvfp4", 9, B=80, H=40, H_kv=40, D=128, block_size=16,
+                 dtype="bf16", lengths="uniform:128,4096", pool="scaled:1.25", kv="nvfp4",
+                 k_scale=0.9, v_scale=1.3, seed_of=3,
+                 description="llama2_13b_b80 with an NVFP4 KV cache"),
     ]
 }
 
@@ -172,6 +185,12 @@ class Step:
     pack_requests: list
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # NVFP4: block scales of the caches and of the new tokens ([..., H_kv, D/16] E4M3 bytes);
+    # k_cache / v_cache / k_new / v_new then hold the packed E2M1 codes ([..., H_kv, D/2])
+    k_bscales: torch.Tensor | None = None
+    v_bscales: torch.Tensor | None = None
+    k_new_bscales: torch.Tensor | None = None
+    v_new_bscales: torch.Tensor | None = None
 
     @property
     def max_context_len(self) -> int:
@@ -233,7 +252,26 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
     gen.manual_seed(int(np.random.default_rng(s_val).integers(0, 2**62)))
     dt = w.torch_dtype
     q = _randn((B, w.H, w.D), gen, device, dt)
-    if w.kv == "fp8":
+    nv = {}
+    if w.kv == "nvfp4":
+        # random E2M1 code pairs (every byte is valid) and E4M3 block scales in [0.25, 0.47)
+        # (exponent field 5), so element values are of order 1
+        def codes(shape):
+            return torch.randint(0, 256, shape, generator=gen, device=device, dtype=torch.int32
+                                 ).to(torch.uint8)
+
+        def bscales(shape):
+            return torch.randint(0x28, 0x30, shape, generator=gen, device=device,
+                                 dtype=torch.int32).to(torch.uint8)
+
+        half, nsc = w.D // 2, w.D // 16
+        k_cache = codes((NB, bs, w.H_kv, half))
+        v_cache = codes((NB, bs, w.H_kv, half))
+        k_new = codes((B, w.H_kv, half))
+        v_new = codes((B, w.H_kv, half))
+        nv = dict(k_bscales=bscales((NB, bs, w.H_kv, nsc)), v_bscales=bscales((NB, bs, w.H_kv, nsc)),
+                  k_new_bscales=bscales((B, w.H_kv, nsc)), v_new_bscales=bscales((B, w.H_kv, nsc)))
+    elif w.kv == "fp8":
         # N(0,1) values stored as E4M3 codes of value / scale (round to nearest even)
         def kvt(shape, sc):
             return _randn(shape, gen, device, torch.float32, scale_by=1.0 / sc,
@@ -254,8 +292,12 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
                 valid[bt[b, t // bs] * bs + t % bs] = True
         bad = torch.from_numpy(~valid).to(device).view(NB, bs)
         nan = 0x7F if w.kv == "fp8" else float("nan")  # 0x7F is the E4M3 NaN code
-        k_cache[bad] = nan
-        v_cache[bad] = nan
+        if w.kv == "nvfp4":  # E2M1 has no NaN: poison the rows' block scales instead
+            nv["k_bscales"][bad] = 0x7F
+            nv["v_bscales"][bad] = 0x7F
+        else:
+            k_cache[bad] = nan
+            v_cache[bad] = nan
 
     order = np.argsort(-L.astype(np.int64), kind="stable")
     pack = [int(b) for b in order[: w.pack_top]] if w.pack_top else []
@@ -270,4 +312,5 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
         pack_requests=pack,
         k_scale=float(np.float32(w.k_scale)),
         v_scale=float(np.float32(w.v_scale)),
+        **nv,
     )

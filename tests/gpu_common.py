@@ -57,14 +57,28 @@ def assert_attention_close(got: torch.Tensor, ref: np.ndarray, what: str = "",
     assert rel.max() <= REL_TOL, f"{what}: max rel err {rel.max():.3e} > {REL_TOL}"
 
 
+def _oracle_attention(s, q, kc, vc, bt, lens, ksc=None, vsc=None, num_threads=0):
+    if s.w.kv == "nvfp4":
+        return orc.paged_decode_attention_nvfp4(q, kc, vc, ksc, vsc, bt, lens, s.scale,
+                                                s.k_scale, s.v_scale, num_threads=num_threads)
+    return orc.paged_decode_attention(q, kc, vc, bt, lens, s.scale, num_threads=num_threads,
+                                      k_scale=s.k_scale, v_scale=s.v_scale)
+
+
 def oracle_full_step(s, append: bool = True, num_threads: int = 0):
-    """fp64 oracle of the whole step on host copies taken before the GPU runs."""
+    """fp64 oracle of the whole step on host copies taken before the GPU runs. For NVFP4
+    the block-scale tensors are appended like the data (both are byte caches)."""
     kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
+    ksc = vsc = None
+    if s.w.kv == "nvfp4":
+        ksc, vsc = to_np(s.k_bscales).copy(), to_np(s.v_bscales).copy()
     if append:
         assert orc.kv_append(to_np(s.k_new), to_np(s.v_new), kc, vc, s.slot_mapping_np) == 0
-    ref, st = orc.paged_decode_attention(to_np(s.q), kc, vc, s.block_tables_np,
-                                         s.context_lens_np, s.scale, num_threads=num_threads,
-                                         k_scale=s.k_scale, v_scale=s.v_scale)
+        if ksc is not None:
+            assert orc.kv_append(to_np(s.k_new_bscales), to_np(s.v_new_bscales), ksc, vsc,
+                                 s.slot_mapping_np) == 0
+    ref, st = _oracle_attention(s, to_np(s.q), kc, vc, s.block_tables_np, s.context_lens_np,
+                                ksc, vsc, num_threads)
     return ref, st, kc, vc
 
 
@@ -80,6 +94,10 @@ def oracle_sampled(s, reqs, append: bool = True):
     idx = torch.tensor(used if used else [0], dtype=torch.long, device=s.k_cache.device)
     kc = to_np(s.k_cache.index_select(0, idx)).copy()
     vc = to_np(s.v_cache.index_select(0, idx)).copy()
+    ksc = vsc = None
+    if s.w.kv == "nvfp4":
+        ksc = to_np(s.k_bscales.index_select(0, idx)).copy()
+        vsc = to_np(s.v_bscales.index_select(0, idx)).copy()
     mb = max(1, max(nblk) if nblk else 1)
     bt = np.full((len(reqs), mb), -1, np.int32)
     for i, (r, n) in enumerate(zip(reqs, nblk)):
@@ -93,10 +111,11 @@ def oracle_sampled(s, reqs, append: bool = True):
                 slots[i] = pos[sl // bs] * bs + sl % bs
         st = orc.kv_append(to_np(s.k_new[reqs]), to_np(s.v_new[reqs]), kc, vc, slots)
         assert st == 0
-    q = to_np(s.q[reqs]).copy()
-    ref, st = orc.paged_decode_attention(q, kc, vc, bt, lens, s.scale, k_scale=s.k_scale,
-                                         v_scale=s.v_scale)
-    return ref, st
+        if ksc is not None:
+            st = orc.kv_append(to_np(s.k_new_bscales[reqs]), to_np(s.v_new_bscales[reqs]), ksc,
+                               vsc, slots)
+            assert st == 0
+    return _oracle_attention(s, to_np(s.q[reqs]).copy(), kc, vc, bt, lens, ksc, vsc)
 
 
 def gpu_step(s, append: bool = True, sm_cap: int = 0, out_dtype=None, workspace=None):
@@ -104,8 +123,16 @@ def gpu_step(s, append: bool = True, sm_cap: int = 0, out_dtype=None, workspace=
     err = torch.zeros(1, dtype=torch.int32, device=s.q.device)
     if append:
         pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+        if s.w.kv == "nvfp4":
+            pda.kv_append(s.k_new_bscales, s.v_new_bscales, s.k_bscales, s.v_bscales,
+                          s.slot_mapping, error_word=err)
     out = torch.empty(s.q.shape, dtype=out_dtype or s.q.dtype, device=s.q.device)
-    if s.k_cache.dtype == torch.uint8:
+    if s.w.kv == "nvfp4":
+        pda.paged_decode_attention_nvfp4(out, s.q, s.k_cache, s.v_cache, s.k_bscales,
+                                         s.v_bscales, s.block_tables, s.context_lens,
+                                         s.max_context_len, s.scale, s.k_scale, s.v_scale,
+                                         sm_cap=sm_cap, workspace=workspace, error_word=err)
+    elif s.w.kv == "fp8":
         pda.paged_decode_attention_fp8(out, s.q, s.k_cache, s.v_cache, s.block_tables,
                                        s.context_lens, s.max_context_len, s.scale, s.k_scale,
                                        s.v_scale, sm_cap=sm_cap, workspace=workspace,

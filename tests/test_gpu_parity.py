@@ -483,3 +483,67 @@ def test_fp8_entry_rejects_plain_caches_and_base_entry_rejects_fp8():
         pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, s.block_tables,
                                    s.context_lens, s.max_context_len, s.scale)
     assert e.value.status == binding.PDA_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ NVFP4 KV cache
+NVFP4_SHAPES = [(128, 32, 32), (128, 32, 8), (128, 16, 2), (128, 64, 8), (64, 16, 4),
+                (64, 16, 16)]
+
+
+@pytest.mark.parametrize("D,H,H_kv", NVFP4_SHAPES)
+def test_nvfp4_shapes_and_groups(D, H, H_kv):
+    w = variant("llama2_13b_b80_nvfp4", D=D, H=H, H_kv=H_kv, B=9, lengths="uniform:1,700")
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, 700, 255], np.int32)
+    s = wl.make_step(w, device=DEV, lengths=lens)
+    ref, st, kc, vc = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
+    assert_attention_close(out, ref, f"nvfp4 D={D} H={H} H_kv={H_kv}")
+
+
+@pytest.mark.parametrize("name,B", [("llama2_13b_b80_nvfp4", 10), ("gqa_skew_b256_nvfp4", 24)])
+def test_nvfp4_reduced_batch_every_output(name, B):
+    s = wl.make_step(name, device=DEV, B=B)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, name, strict=True)
+
+
+def test_nvfp4_full_size_sampled():
+    s = wl.make_step("gqa_skew_b256_nvfp4", device=DEV)
+    reqs = _sample(s)
+    ref, st = oracle_sampled(s, reqs)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out[reqs], ref, "gqa_skew_b256_nvfp4", strict=True)
+
+
+def test_nvfp4_empty_single_and_poisoned_scales():
+    lens = np.array([0, 1, 2, 16, 17, 40], np.int32)
+    s = wl.make_step("llama2_13b_b80_nvfp4", device=DEV, lengths=lens, B=6, poison_unused=True)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0 and np.isfinite(ref).all()
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert_attention_close(out, ref, "nvfp4 edge cases")
+    assert (out[0] == 0).all()
+
+
+def test_nvfp4_pack_of_data_and_scales_is_bit_exact():
+    s = wl.make_step("gqa_skew_b256_nvfp4", device=DEV, B=8)
+    r = int(np.argmax(s.context_lens_np))
+    L = int(s.context_lens_np[r])
+    n = (L + 15) // 16
+    blocks = torch.from_numpy(s.block_tables_np[r, :n].astype(np.int64)).to(DEV)
+    for data_k, data_v in ((s.k_cache, s.v_cache), (s.k_bscales, s.v_bscales)):
+        packed = torch.empty((L, 2) + tuple(data_k.shape[2:]), dtype=torch.uint8, device=DEV)
+        pda.kv_pack_blocks(packed, data_k, data_v, s.block_tables[r], L)
+        want, st = orc.kv_pack_blocks(to_np(data_k.index_select(0, blocks)).copy(),
+                                      to_np(data_v.index_select(0, blocks)).copy(),
+                                      np.arange(n, dtype=np.int32), L)
+        assert st == 0 and np.array_equal(to_np(packed), want)

@@ -7,9 +7,18 @@ from paged_decode_attention_02_gb300 import workloads as wl
 
 
 def test_named_workloads():
-    assert [wl.get(i).name for i in range(1, 8)] == [
+    assert [wl.get(i).name for i in range(1, 10)] == [
         "tiny", "llama2_7b_b8", "llama2_13b_b80", "gqa_skew_b256", "sm_sweep_b128",
-        "gqa_skew_b256_fp8", "llama2_13b_b80_fp8"]
+        "gqa_skew_b256_fp8", "llama2_13b_b80_fp8", "gqa_skew_b256_nvfp4",
+        "llama2_13b_b80_nvfp4"]
+
+
+def test_nvfp4_workload_has_codes_and_block_scales():
+    s = wl.make_step("llama2_13b_b80_nvfp4", B=2)
+    w = s.w
+    assert s.k_cache.shape[-1] == w.D // 2 and s.k_bscales.shape[-1] == w.D // 16
+    assert s.k_new.shape == (2, w.H_kv, w.D // 2) and s.k_new_bscales.shape == (2, w.H_kv, w.D // 16)
+    assert int(s.k_bscales.min()) >= 0x28 and int(s.k_bscales.max()) < 0x30
 
 
 def test_fp8_workload_shares_lengths_and_tables_with_its_twin():
