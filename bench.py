@@ -251,12 +251,24 @@ def oracle_pass(s, threads: int):
     from oracle import oracle as orc
     kc, vc = _np(s.k_cache).copy(), _np(s.v_cache).copy()
     q, kn, vn = _np(s.q), _np(s.k_new), _np(s.v_new)
+    nvfp4 = s.w.kv == "nvfp4"
+    if nvfp4:  # codes and block scales are appended and packed as two byte arrays
+        ksc, vsc = _np(s.k_bscales).copy(), _np(s.v_bscales).copy()
+        ksn, vsn = _np(s.k_new_bscales), _np(s.v_new_bscales)
     t0 = time.perf_counter()
     orc.kv_append(kn, vn, kc, vc, s.slot_mapping_np)
-    orc.paged_decode_attention(q, kc, vc, s.block_tables_np, s.context_lens_np, s.scale,
-                               num_threads=threads)
+    if nvfp4:
+        orc.kv_append(ksn, vsn, ksc, vsc, s.slot_mapping_np)
+        orc.paged_decode_attention_nvfp4(q, kc, vc, ksc, vsc, s.block_tables_np,
+                                         s.context_lens_np, s.scale, s.k_scale, s.v_scale,
+                                         num_threads=threads)
+    else:
+        orc.paged_decode_attention(q, kc, vc, s.block_tables_np, s.context_lens_np, s.scale,
+                                   num_threads=threads, k_scale=s.k_scale, v_scale=s.v_scale)
     for r in s.pack_requests:
         orc.kv_pack_blocks(kc, vc, s.block_tables_np[r], int(s.context_lens_np[r]))
+        if nvfp4:
+            orc.kv_pack_blocks(ksc, vsc, s.block_tables_np[r], int(s.context_lens_np[r]))
     return time.perf_counter() - t0
 
 
