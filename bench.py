@@ -42,7 +42,9 @@ HEADLINE = "gqa_skew_b256"
 METRIC = "paged decode-attn HBM GB/s (% of GB300 peak) and decode tokens/s per layer"
 FALLBACK_HBM_GBS = 6800.0
 ATTN_SOURCES = ["paged_decode_attention_02_gb300/csrc/decode_attention.cu",
-                "paged_decode_attention_02_gb300/csrc/pda_device.cuh"]
+                "paged_decode_attention_02_gb300/csrc/pda_device.cuh",
+                "paged_decode_attention_02_gb300/csrc/warp_attn_tc.cuh",
+                "paged_decode_attention_02_gb300/csrc/pda_api.cu"]
 
 
 # ------------------------------------------------------------------ bytes
@@ -239,6 +241,25 @@ def barrier(ws):
         dist.barrier()
 
 
+def kv_arrays(s):
+    """(cache K, cache V, new K, new V) byte arrays of a step: the codes, and for NVFP4 the
+    block scales too (appended, packed and unpacked as arrays of their own)."""
+    arrays = [(s.k_cache, s.v_cache, s.k_new, s.v_new)]
+    if s.w.kv == "nvfp4":
+        arrays.append((s.k_bscales, s.v_bscales, s.k_new_bscales, s.v_new_bscales))
+    return arrays
+
+
+def workspace_for(s, sm_cap):
+    import paged_decode_attention_02_gb300 as pda
+    w = s.w
+    if w.kv == "nvfp4":
+        return pda.binding.nvfp4_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, sm_cap,
+                                           s.q.device)
+    return pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype, sm_cap,
+                               s.q.device)
+
+
 # ------------------------------------------------------------------ oracle (CPU) timing
 def _np(t):
     import torch
@@ -328,26 +349,32 @@ def run_ours(args, ws, rank, local):
 
     out = torch.empty_like(s.q)
     cap = args.sm_cap
-    wsp = pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype, cap, dev)
+    wsp = workspace_for(s, cap)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    packs = [torch.empty((int(s.context_lens_np[r]), 2, w.H_kv, w.D), dtype=w.kv_torch_dtype,
-                         device=dev) for r in pack_reqs]
+    # (cache K, cache V, new K, new V): the codes, and for NVFP4 also the block scales, each
+    # appended and packed as its own byte array
+    arrays = kv_arrays(s)
     pack_rows = [s.block_tables[r] for r in pack_reqs]
     pack_lens = [int(s.context_lens_np[r]) for r in pack_reqs]
-    launches_per_step = 1 + 2 + (1 if pack_reqs else 0)
+    packs_of = [[torch.empty((L, 2) + tuple(kc.shape[2:]), dtype=kc.dtype, device=dev)
+                 for L in pack_lens] for kc, _, _, _ in arrays]
+    packs = [p for group in packs_of for p in group]
+    launches_per_step = len(arrays) + 1 + (len(arrays) if pack_reqs else 0)
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
+        for kc, vc, kn, vn in arrays:
+            pda.kv_append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
         if ev:
             ev[1].record(stream)
         attention(s, out, cap, wsp, error_word=err)
         if ev:
             ev[2].record(stream)
         if pack_reqs:
-            pda.kv_pack_blocks_batched(packs, s.k_cache, s.v_cache, pack_rows, pack_lens,
-                                       error_word=err)
+            for (kc, vc, _, _), group in zip(arrays, packs_of):
+                pda.kv_pack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
+                                           error_word=err)
         if ev:
             ev[3].record(stream)
 
@@ -379,9 +406,9 @@ def run_ours(args, ws, rank, local):
     t_step_max = dist_max(t_step, ws)
 
     # ---- end to end: per-step inputs from pinned host memory, results back to host
-    h_in = [x.detach().cpu().pin_memory() for x in
-            (s.q, s.k_new, s.v_new, s.slot_mapping, s.block_tables, s.context_lens)]
-    d_in = [s.q, s.k_new, s.v_new, s.slot_mapping, s.block_tables, s.context_lens]
+    d_in = [s.q] + [t for _, _, kn, vn in arrays for t in (kn, vn)] + [
+        s.slot_mapping, s.block_tables, s.context_lens]
+    h_in = [x.detach().cpu().pin_memory() for x in d_in]
     h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory()] + [
         torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in packs]
     d_out = [out] + packs
@@ -423,8 +450,9 @@ def run_ours(args, ws, rank, local):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             flush()
             a.record(stream)
-            pda.kv_unpack_blocks_batched(packs, s.k_cache, s.v_cache, pack_rows, pack_lens,
-                                         error_word=err)
+            for (kc, vc, _, _), group in zip(arrays, packs_of):
+                pda.kv_unpack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
+                                             error_word=err)
             b.record(stream)
             uev.append((a, b))
         torch.cuda.synchronize()
@@ -444,7 +472,9 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        # arithmetic type: fp32 on the CUDA cores; quantised caches at D = 128 multiply fp16
+        # operands (exact codes, split probabilities) on the tensor cores into fp32
+        "dtype": "f16 mma, f32 accumulate" if (w.kv and w.D == 128) else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": s.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
                    "block_size": w.block_size, "kv_dtype": w.kv or w.dtype,
@@ -466,8 +496,8 @@ def run_ours(args, ws, rank, local):
                     "bytes": nb["pack"], "note": "not part of the step"} if t_unpack else None),
         "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": traffic, "kernel": "paged_decode_attention call "
-                     "(attn_partial_kernel + attn_combine_kernel)", "peak_source": peak_src},
+                     "traffic": traffic, "kernel": "attn_partial_kernel (one launch per call; "
+                     "cut segments are merged inside it)", "peak_source": peak_src},
         "e2e": {"value": round(replica_value(nb["step"], t_e2e, ws), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -519,10 +549,7 @@ def sweep_workloads(args, dev, flush, peak):
         res_w = {}
         for cap in caps:
             out = torch.empty_like(s.q)
-            wsp = (pda.binding.nvfp4_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, cap, dev)
-                   if w.kv == "nvfp4" else
-                   pda.alloc_workspace(s.B, w.H, w.H_kv, w.D, w.block_size, w.kv_torch_dtype,
-                                       cap, dev))
+            wsp = workspace_for(s, cap)
             for _ in range(3):
                 flush()
                 attention(s, out, cap, wsp)

@@ -27,8 +27,11 @@
 //    with a log-sum-exp combine, so no second kernel is needed. This is the split and merge
 //    of Orca's iteration-level batching (page "Disaggregated LLM Serving", sec. 2.1),
 //    applied along the sequence.
-//  * No tensor cores: per kv-head and token this is G dot products of length D against
-//    2 * D * sizeof(elem) bytes, far below the tensor-core break-even.
+//  * bf16 and fp32 caches run on the CUDA cores: per kv-head and token this is G dot
+//    products of length D against 2 * D * sizeof(elem) bytes, and the bf16 path already
+//    streams at the HBM rate. Quantised caches (FP8, NVFP4) at D = 128 carry two to four
+//    times as many tokens per byte, so their dot products go to the tensor cores
+//    (warp_attn_tc.cuh); the pipeline, scheduling and merge below are shared.
 #include <math.h>
 
 #include <atomic>
@@ -40,6 +43,7 @@
 
 #include "pda_device.cuh"
 #include "pda_internal.h"
+#include "warp_attn_tc.cuh"
 
 namespace pda {
 
@@ -50,11 +54,21 @@ namespace pda {
 #define PDA_ATTN_MAX_STAGES 4  // most pipeline stages per warp
 #endif
 
+#ifndef PDA_TC_WARPS
+#define PDA_TC_WARPS 12        // warps (workers) per block of the tensor-core tile step
+#endif
+
 constexpr int kBS = 16;             // tokens per physical block (box height of the TMA)
-constexpr int kMaxWarps = PDA_ATTN_WARPS;
-// Warps per block for a GQA group of G: the group of 8 keeps 8 warps so its 8 heads of q
-// and o stay in registers (up to 255 per thread).
-__host__ __device__ constexpr int warps_for_group(int G) { return G >= 8 ? 8 : kMaxWarps; }
+constexpr int kMaxWarps = PDA_ATTN_WARPS > PDA_TC_WARPS ? PDA_ATTN_WARPS : PDA_TC_WARPS;
+// Warps per block for a GQA group of G: on the CUDA cores the group of 8 keeps 8 warps so
+// its 8 heads of q and o stay in registers (up to 255 per thread); the tensor-core tile
+// step holds q and o in mma fragments and keeps all warps.
+__host__ __device__ constexpr int warps_for_group(int G, bool tc) {
+  return tc ? PDA_TC_WARPS : (G >= 8 ? 8 : PDA_ATTN_WARPS);
+}
+// Stage alignment: the tensor-core step reads TMA tiles written with the 128-byte (FP8) or
+// 64-byte (NVFP4) swizzle, whose pattern repeats every 1024 (512) bytes.
+__host__ __device__ constexpr int stage_align(bool tc) { return tc ? 1024 : 128; }
 constexpr int kMetaBytesPerWarp = 2 * 32 * 8;  // two groups of 32 (block id, length) pairs
 constexpr int kMaxBatch = 8192;     // prefix table size bound (shared memory)
 constexpr int kSmemBudget = 226 * 1024;  // dynamic bytes; static shared memory sits on top
@@ -337,13 +351,40 @@ struct WarpAttn {
   __device__ __forceinline__ float o(int j, int e) const {
     return (e & 1) ? o2[j][e >> 1].y : o2[j][e >> 1].x;
   }
+
+  // Calls f(head, d, values, VEC, l of the head) for each run of output elements this lane
+  // writes (lanes of row group 0 hold the reduced state); lj as filled by reduce().
+  template <typename F>
+  __device__ __forceinline__ void for_each_out(const float* lj, F&& f) const {
+    if (rw != 0) return;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float v[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[e] = o(j, e);
+      f(j, cl * VEC, v, VEC, lj[j]);
+    }
+  }
+  __device__ __forceinline__ bool writes_ml(int lane_) const { return lane_ == 0; }
 };
+
+// n fp32 values (n = 2 or a multiple of 4, p aligned to n * 4 bytes up to 16).
+__device__ __forceinline__ void store_f32(float* p, const float* v, int n) {
+  if (n == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    return;
+  }
+  for (int e = 0; e < n; e += 4)
+    *reinterpret_cast<float4*>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+}
 
 __device__ __forceinline__ void store_out(void* out, size_t off, const float* v, int n,
                                           int out_bf16) {
   if (out_bf16) {
     __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + off;
-    if (n == 8) {
+    if (n == 2) {
+      *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
+    } else if (n == 8) {
       uint4 w;
       __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
       __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
@@ -358,9 +399,7 @@ __device__ __forceinline__ void store_out(void* out, size_t off, const float* v,
       for (int e = 0; e < n; ++e) p[e] = __float2bfloat16_rn(v[e]);
     }
   } else {
-    float* p = reinterpret_cast<float*>(out) + off;
-    for (int e = 0; e < n; e += 4)
-      *reinterpret_cast<float4*>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    store_f32(reinterpret_cast<float*>(out) + off, v, n);
   }
 }
 
@@ -477,14 +516,21 @@ __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1,
     merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, W_tiles, NW, lane);
 }
 
-template <typename KV, typename QT, int D, int G>
-__global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
+// TC selects the tile step: the tensor-core one (quantised caches, D = 128) or the
+// CUDA-core one.
+template <typename KV, typename QT, int D, int G, bool TC>
+__global__ void __launch_bounds__(warps_for_group(G, TC) * 32, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Geo = Geometry<KV, QT, D, G>;
-  using W = WarpAttn<KV, QT, D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  if ((smem_addr(smem) & 127u) != 0) {  // TMA destinations below assume 128-byte alignment
+  using W = std::conditional_t<TC, WarpAttnTC<KV, D, G>, WarpAttn<KV, QT, D, G>>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // The host reserves stage_align(TC) - 128 spare bytes; the layout starts at the first
+  // aligned address (swizzled TMA tiles need the swizzle period's alignment).
+  constexpr uint32_t kAlign = stage_align(TC);
+  unsigned char* smem =
+      smem_raw + ((kAlign - (smem_addr(smem_raw) & (kAlign - 1))) & (kAlign - 1));
+  if ((smem_addr(smem_raw) & 127u) != 0) {  // TMA destinations assume 128-byte alignment
     if (threadIdx.x == 0) atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
     return;
   }
@@ -736,36 +782,29 @@ __global__ void __launch_bounds__(warps_for_group(G) * 32, 1)
       const int seg_end = seg_start + cnb;
       const bool complete = seg_start >= t_begin && seg_end <= t_end;
       if (complete) {
-        if (st.rw == 0) {
+        st.for_each_out(lj, [&](int j, int d, const float* o, int n, float l) {
+          float v[8];
+          const float inv = seg_bad ? __int_as_float(0x7fc00000) : p.v_scale / l;
 #pragma unroll
-          for (int j = 0; j < G; ++j) {
-            float v[W::VEC];
-            const float inv = seg_bad ? __int_as_float(0x7fc00000) : p.v_scale / lj[j];
-#pragma unroll
-            for (int e = 0; e < W::VEC; ++e) v[e] = st.o(j, e) * inv;
-            const size_t off =
-                (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D +
-                st.cl * W::VEC;
-            store_out(p.out, off, v, W::VEC, p.out_bf16);
-          }
-        }
+          for (int e = 0; e < 8; ++e)
+            if (e < n) v[e] = o[e] * inv;
+          const size_t off =
+              (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D + d;
+          store_out(p.out, off, v, n, p.out_bf16);
+        });
       } else {
         // A piece of a segment cut by a range boundary: store (m, l, o), register it, and
         // merge the segment if this was its last piece.
         const int slot = 2 * w + (seg_start <= t_begin ? 0 : 1);
-        if (st.rw == 0) {
+        st.for_each_out(lj, [&](int j, int d, const float* o, int n, float) {
+          store_f32(p.ws_o + (static_cast<size_t>(slot) * G + j) * D + d, o, n);
+        });
+        if (st.writes_ml(lane)) {
 #pragma unroll
           for (int j = 0; j < G; ++j) {
-            float* dst = p.ws_o + (static_cast<size_t>(slot) * G + j) * D + st.cl * W::VEC;
-#pragma unroll
-            for (int e = 0; e < W::VEC; e += 4)
-              *reinterpret_cast<float4*>(dst + e) =
-                  make_float4(st.o(j, e), st.o(j, e + 1), st.o(j, e + 2), st.o(j, e + 3));
-            if (st.cl == 0) {
-              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
-              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
-                  seg_bad ? __int_as_float(0x7fc00000) : lj[j];
-            }
+            p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
+            p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
+                seg_bad ? __int_as_float(0x7fc00000) : lj[j];
           }
         }
         __threadfence();  // this lane's piece stores before the arrival below
@@ -819,23 +858,29 @@ size_t q_bytes_for(pda_dtype kv) {
   return (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4) ? 2u : dtype_bytes(kv);
 }
 
+// Quantised caches at D = 128 take the tensor-core tile step.
+bool use_tc(pda_dtype kv, int D) { return (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4) && D == 128; }
+
 // One pipeline stage: the K and V tiles, (NVFP4) their block scales, the q rows.
 uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
   const size_t tile = kv == PDA_NVFP4 ? kBS * D / 2 : kBS * D * dtype_bytes(kv);
   const size_t scales = kv == PDA_NVFP4 ? 2 * kBS * D / 16 : 0;
   const size_t q = static_cast<size_t>(G) * D * q_bytes_for(kv);
-  return static_cast<uint32_t>(round_up(2 * tile + scales + q, 128));
+  return static_cast<uint32_t>(round_up(2 * tile + scales + q, stage_align(use_tc(kv, D))));
 }
 
 bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
                LaunchPlan* pl) {
+  const bool tc = use_tc(kv, D);
+  const size_t align = stage_align(tc);
   pl->stage_bytes = stage_bytes_for(kv, D, G);
-  pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, 128));
-  const size_t fixed = pl->prefix_bytes + 8;  // + alignment of the metadata ring
+  pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, align));
+  // + alignment of the metadata ring, + room to align the layout's start
+  const size_t fixed = pl->prefix_bytes + 8 + (align - 128);
   if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
   pl->nwarps = 0;
   // The most warps that still get two stages each; then as many stages as fit.
-  for (int nw = warps_for_group(G); nw >= 2; --nw) {
+  for (int nw = warps_for_group(G, tc); nw >= 2; --nw) {
     const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
     const size_t meta = static_cast<size_t>(nw) * kMetaBytesPerWarp;
     if (fixed + meta >= static_cast<size_t>(kSmemBudget)) continue;
@@ -865,13 +910,13 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnParams);
 
-template <typename KV, typename QT, int D>
+template <typename KV, typename QT, int D, bool TC = false>
 KernelFn pick_g(int G) {
   switch (G) {
-    case 1: return attn_partial_kernel<KV, QT, D, 1>;
-    case 2: return attn_partial_kernel<KV, QT, D, 2>;
-    case 4: return attn_partial_kernel<KV, QT, D, 4>;
-    case 8: return attn_partial_kernel<KV, QT, D, 8>;
+    case 1: return attn_partial_kernel<KV, QT, D, 1, TC>;
+    case 2: return attn_partial_kernel<KV, QT, D, 2, TC>;
+    case 4: return attn_partial_kernel<KV, QT, D, 4, TC>;
+    case 8: return attn_partial_kernel<KV, QT, D, 8, TC>;
     default: return nullptr;
   }
 }
@@ -881,10 +926,10 @@ KernelFn pick_kernel(pda_dtype kv, int D, int G) {
     if (D == 128) return pick_g<__nv_bfloat16, __nv_bfloat16, 128>(G);
     if (D == 64) return pick_g<__nv_bfloat16, __nv_bfloat16, 64>(G);
   } else if (kv == PDA_FP8_E4M3) {
-    if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128>(G);
+    if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128, true>(G);
     if (D == 64) return pick_g<fp8e4m3, __nv_bfloat16, 64>(G);
   } else if (kv == PDA_NVFP4) {
-    if (D == 128) return pick_g<nvfp4, __nv_bfloat16, 128>(G);
+    if (D == 128) return pick_g<nvfp4, __nv_bfloat16, 128, true>(G);
     if (D == 64) return pick_g<nvfp4, __nv_bfloat16, 64>(G);
   } else {
     if (D == 128) return pick_g<float, float, 128>(G);
@@ -917,10 +962,10 @@ pda_status allow_max_smem(const void* fn, int dev) {
 // The last few encoded KV tensor maps, keyed by everything the encoding depends on.
 struct MapKey {
   const void* base;
-  int num_blocks, block_size, H_kv, D, dtype;
+  int num_blocks, block_size, H_kv, D, dtype, swizzle;
   bool operator==(const MapKey& o) const {
     return base == o.base && num_blocks == o.num_blocks && block_size == o.block_size &&
-           H_kv == o.H_kv && D == o.D && dtype == o.dtype;
+           H_kv == o.H_kv && D == o.D && dtype == o.dtype && swizzle == o.swizzle;
   }
 };
 constexpr int kMapCache = 8;
@@ -930,8 +975,10 @@ CUtensorMap g_map_val[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
 pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
-                                int block_size, int H_kv, int D, pda_dtype dtype) {
-  const MapKey key{base, num_blocks, block_size, H_kv, D, static_cast<int>(dtype)};
+                                int block_size, int H_kv, int D, pda_dtype dtype,
+                                int swizzle_bytes) {
+  const MapKey key{base, num_blocks, block_size, H_kv, D, static_cast<int>(dtype),
+                   swizzle_bytes};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_map_used; ++i)
@@ -940,7 +987,8 @@ pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
         return PDA_OK;
       }
   }
-  const pda_status st = encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype);
+  const pda_status st =
+      encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype, swizzle_bytes);
   if (st != PDA_OK) return st;
   std::lock_guard<std::mutex> lock(g_map_mu);
   g_map_key[g_map_next] = key;
@@ -1026,13 +1074,17 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
   if (st != PDA_OK) return st;
 
-  // the TMA sees an NVFP4 row as D/2 bytes
+  // the TMA sees an NVFP4 row as D/2 bytes; the tensor-core step reads swizzled tiles whose
+  // swizzle span is one whole row (128 bytes FP8, 64 bytes NVFP4)
   const int row_elems = kv_dtype == PDA_NVFP4 ? D / 2 : D;
   const pda_dtype map_type = kv_dtype == PDA_NVFP4 ? PDA_FP8_E4M3 : kv_dtype;
+  const int swizzle = use_tc(kv_dtype, D) ? row_elems : 0;
   CUtensorMap tmK, tmV;
-  st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, row_elems, map_type);
+  st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, row_elems, map_type,
+                            swizzle);
   if (st != PDA_OK) return st;
-  st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, row_elems, map_type);
+  st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, row_elems, map_type,
+                            swizzle);
   if (st != PDA_OK) return st;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);

@@ -47,7 +47,10 @@ pda_status current_device_sms(int* device, int* num_sms) {
 }
 
 pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
-                                int block_size, int H_kv, int D, pda_dtype dtype) {
+                                int block_size, int H_kv, int D, pda_dtype dtype,
+                                int swizzle_bytes) {
+  if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128)
+    return PDA_ERR_INVALID_ARG;
   std::call_once(g_encode_once, load_encoder);
   if (g_encode == nullptr) return PDA_ERR_CUDA;
   const cuuint64_t e = dtype_bytes(dtype);
@@ -60,9 +63,23 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
   const CUtensorMapDataType dt = dtype == PDA_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                  : dtype == PDA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  // With a swizzle the row (box width) must equal the swizzle span: 16-byte chunk c of
+  // row r of the box then lands at chunk c ^ (r & 7) (128 B) or c ^ ((r >> 1) & 3) (64 B).
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_bytes != 0 && static_cast<cuuint64_t>(D) * e != static_cast<cuuint64_t>(swizzle_bytes))
+    return PDA_ERR_INVALID_ARG;
+  // L2 fills no wider than a row: rows of one kv-head are H_kv rows apart, and a wider fill
+  // drags in the neighbouring heads' rows, which other warps read much later (256-byte
+  // fills on 64-byte rows read four times the bytes from DRAM).
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * e;
+  const CUtensorMapL2promotion promo = row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                       : row_bytes >= 64  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                          : CU_TENSOR_MAP_L2_PROMOTION_NONE;
   const CUresult r = g_encode(tm, dt, 3, const_cast<void*>(base), dims, strides, box,
-                              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
 }

@@ -262,6 +262,78 @@ struct Elem<nvfp4> {
   }
 };
 
+// ---------------------------------------------------------------- tensor-core helpers
+// D += A * B for one 16x8x16 tile, fp16 operands, fp32 accumulators (register fragments).
+// a: rows (g, g+8) x k pairs (2t, 2t+8) as four f16x2 words; b: k pairs (2t, 2t+8) of
+// column g; d/c: (row g, cols 2t, 2t+1), (row g+8, cols 2t, 2t+1), with g = lane / 4 and
+// t = lane % 4.
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 matrices of 16-bit elements from shared memory, transposed: lane 8i + j gives
+// the address of row j of matrix i; afterwards word i of lane (g, t) holds elements
+// (row 2t, col g) in its low half and (row 2t + 1, col g) in its high half.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(row_addr))
+               : "memory");
+}
+
+// Byte permute: byte i of the result is byte sel_i (0-7) of the pair {a, b}.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Four E4M3 codes -> two f16x2 words (codes 0,1 -> lo; codes 2,3 -> hi), exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Two E4M3 codes in the low 16 bits of w -> one f16x2 word (low byte -> low half), exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 l, u;\n\t"
+      "mov.b32 {l, u}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+      : "=r"(h)
+      : "r"(w));
+  return h;
+}
+
+// Eight E2M1 codes (four bytes, even element in each low nibble) -> four f16x2 words,
+// word i holding the two codes of byte i (low nibble -> low half), exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t* h) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t f16x2_bits(__half2 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ __half2 as_half2(uint32_t w) {
+  return *reinterpret_cast<__half2*>(&w);
+}
+
 // Address of element `off` of a row of T that starts at `base`.
 template <typename T>
 __device__ __forceinline__ const void* elem_ptr(const void* base, int off) {

@@ -14,9 +14,12 @@ namespace pda {
 pda_status current_device_sms(int* device, int* num_sms);
 
 // Encodes a 3-D tiled tensor map over a KV cache [num_blocks * block_size, H_kv, D]
-// (innermost first: D, H_kv, rows) with box {D, 1, block_size}.
+// (innermost first: D, H_kv, rows) with box {D, 1, block_size}. swizzle_bytes is 0 (rows
+// land as they are) or 64 / 128 (the shared-memory swizzle of that span, which must equal
+// the row's byte width).
 pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
-                                int block_size, int H_kv, int D, pda_dtype dtype);
+                                int block_size, int H_kv, int D, pda_dtype dtype,
+                                int swizzle_bytes);
 
 inline size_t dtype_bytes(pda_dtype t) {
   return t == PDA_BF16 ? 2u : (t == PDA_FP8_E4M3 ? 1u : 4u);

@@ -547,3 +547,57 @@ def test_nvfp4_pack_of_data_and_scales_is_bit_exact():
                                       to_np(data_v.index_select(0, blocks)).copy(),
                                       np.arange(n, dtype=np.int32), L)
         assert st == 0 and np.array_equal(to_np(packed), want)
+
+
+# ------------------------------------------------------------------ tensor-core tile step
+# FP8 and NVFP4 caches at D = 128 run their dot products on the tensor cores with fp16
+# operands: q is brought into fp16 range by a power-of-two shift, and a head's running
+# maximum may lag the true one by up to 2^8 before the output is rescaled.
+QUANTISED = ["gqa_skew_b256_fp8", "llama2_13b_b80_fp8", "gqa_skew_b256_nvfp4",
+             "llama2_13b_b80_nvfp4"]
+
+
+@pytest.mark.parametrize("name", QUANTISED)
+def test_tc_q_far_outside_fp16_range(name):
+    """q times 2^20 (|q| up to ~4e6, far above fp16's 65504) with the scale times 2^-20 is
+    the same attention; both sides get the scaled inputs."""
+    s = wl.make_step(name, device=DEV, B=6)
+    s.q.mul_(2.0 ** 20)
+    s.scale = float(np.float32(s.scale) * np.float32(2.0 ** -20))
+    assert s.q.abs().max().item() > 65504
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, f"{name} q x 2^20")
+
+
+@pytest.mark.parametrize("name", QUANTISED)
+@pytest.mark.parametrize("boost", [8.0, 40.0])
+def test_tc_sharp_softmax_rescales(name, boost):
+    """A scale `boost` times larger spreads the scores over tens of log2 units, so later
+    tiles often raise a head's maximum by more than the allowed lag (output rescaled) and
+    others stay within it (probabilities above 1 accumulate unrescaled)."""
+    s = wl.make_step(name, device=DEV, B=8)
+    s.scale = float(np.float32(s.scale) * np.float32(boost))
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, f"{name} scale x {boost}")
+
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("H,H_kv", [(64, 8), (16, 8), (8, 8)])
+def test_tc_groups_with_ragged_tails(kv, H, H_kv):
+    """Every group size on the tensor-core path, lengths that end at every offset of a
+    block (partial tiles mask tokens 1..15 of the last block)."""
+    base = "gqa_skew_b256_fp8" if kv == "fp8" else "gqa_skew_b256_nvfp4"
+    lens = np.array(list(range(1, 17)) + [47, 64, 65, 333], np.int32)
+    w = variant(base, H=H, H_kv=H_kv, B=len(lens), lengths="uniform:1,400")
+    s = wl.make_step(w, device=DEV, lengths=lens, poison_unused=True)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0 and np.isfinite(ref).all()
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert_attention_close(out, ref, f"{kv} H={H} H_kv={H_kv} ragged")
