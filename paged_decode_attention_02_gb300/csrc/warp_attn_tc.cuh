@@ -1,8 +1,8 @@
 // warp_attn_tc.cuh -- one warp's tile step on the tensor cores, for quantised caches
 // (FP8 E4M3, and NVFP4: E2M1 codes with one E4M3 scale per 16 elements) at D = 128.
 //
-// A tile is one physical block (16 tokens) of one kv-head; the G <= 8 query heads of that
-// kv-head go through it together. Per tile the warp computes, with mma.sync m16n8k16
+// A tile is one physical block (16 tokens) of one kv-head; the G (2 to 8) query heads of
+// that kv-head go through it together. Per tile the warp computes, with mma.sync m16n8k16
 // (fp16 operands, fp32 accumulators):
 //   S  = Q K^T    M = heads (G real, padded to 16), N = 16 tokens (two n-tiles), K = d;
 //   O^T += V^T P^T  M = d (eight m-tiles of 16), N = heads (8), K = 16 tokens.
@@ -43,7 +43,7 @@ namespace pda {
 template <typename KV, int D, int G>
 struct WarpAttnTC {
   static_assert(D == 128, "tensor-core tile step is laid out for D = 128");
-  static_assert(G == 1 || G == 2 || G == 4 || G == 8, "at most 8 heads per kv-head");
+  static_assert(G == 2 || G == 4 || G == 8, "2 to 8 heads per kv-head (G = 1 is a GEMV)");
   static constexpr bool FP4 = std::is_same<KV, nvfp4>::value;
   static_assert(FP4 || std::is_same<KV, fp8e4m3>::value, "quantised caches only");
   static constexpr int ROW_BYTES = FP4 ? D / 2 : D;  // bytes of one K or V row

@@ -550,9 +550,10 @@ def test_nvfp4_pack_of_data_and_scales_is_bit_exact():
 
 
 # ------------------------------------------------------------------ tensor-core tile step
-# FP8 and NVFP4 caches at D = 128 run their dot products on the tensor cores with fp16
-# operands: q is brought into fp16 range by a power-of-two shift, and a head's running
-# maximum may lag the true one by up to 2^8 before the output is rescaled.
+# FP8 and NVFP4 caches at D = 128 with G >= 2 run their dot products on the tensor cores
+# with fp16 operands: q is brought into fp16 range by a power-of-two shift, and a head's
+# running maximum may lag the true one by up to 2^8 before the output is rescaled. The
+# G = 1 workloads below take the CUDA-core path and check the same edge cases there.
 QUANTISED = ["gqa_skew_b256_fp8", "llama2_13b_b80_fp8", "gqa_skew_b256_nvfp4",
              "llama2_13b_b80_nvfp4"]
 
@@ -590,8 +591,8 @@ def test_tc_sharp_softmax_rescales(name, boost):
 @pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
 @pytest.mark.parametrize("H,H_kv", [(64, 8), (16, 8), (8, 8)])
 def test_tc_groups_with_ragged_tails(kv, H, H_kv):
-    """Every group size on the tensor-core path, lengths that end at every offset of a
-    block (partial tiles mask tokens 1..15 of the last block)."""
+    """Group sizes 8 and 2 (tensor cores) and 1 (CUDA cores), lengths that end at every
+    offset of a block (partial tiles mask tokens 1..15 of the last block)."""
     base = "gqa_skew_b256_fp8" if kv == "fp8" else "gqa_skew_b256_nvfp4"
     lens = np.array(list(range(1, 17)) + [47, 64, 65, 333], np.int32)
     w = variant(base, H=H, H_kv=H_kv, B=len(lens), lengths="uniform:1,400")
