@@ -508,6 +508,7 @@ def run_ours(args, ws, rank, local):
 
     if args.sweeps and ws == 1:
         res["workloads"] = sweep_workloads(args, dev, flush, peak)
+        res["kv_transfer_staging"] = transfer_legs(dev)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
         sample = oracle_sample(w, args.cpu_seconds, threads)
@@ -525,6 +526,101 @@ def run_ours(args, ws, rank, local):
                       f"{len(sample.pack_requests)}), fp64 C oracle, {reps} pass(es) on "
                       f"{threads} threads in {t_cpu:.1f} s; one pass on 1 thread in "
                       f"{t_one:.1f} s"}
+    return res
+
+
+def transfer_legs(dev, n_layers: int = 40, prompts=(2048, 8192), reps: int = 5) -> dict:
+    """KV transfer staging of one prefilled request, request level against layer level.
+
+    Geometry of llama2-13b (40 layers, 40 kv-heads, D = 128, bf16); the prompt's blocks are
+    scattered over a per-layer pool. Each layer's prefill compute is stood in for by one bf16
+    GEMM with that layer's projection and MLP flops (2 * T * 5120 * 61952; a library GEMM,
+    not part of the measured kernels). Staging a layer = packing its blocks into a dense
+    buffer (our kernel) and handing that buffer on: a device-to-host copy into pinned memory
+    on the copy engine stands in for the send to the decode instance. Times, from the first
+    GEMM on the compute stream: compute alone; compute, then pack and send of every layer
+    (request level: one ``kv_pack_layers`` launch); compute with layer n packed and sent on a
+    transfer stream right after GEMM n (layer level). Reported: each total and the staging
+    time it leaves exposed beyond compute alone (medians of ``reps`` runs)."""
+    import torch
+
+    from paged_decode_attention_02_gb300 import transfer as tr
+
+    H_kv, D, hidden, ffn_out = 40, 128, 5120, 61952
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    gd = torch.Generator(device=dev).manual_seed(1234)  # bulk data drawn on the device
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=gd, device=dev, dtype=torch.bfloat16)
+
+    W = randn(hidden, ffn_out) * 0.01
+    res = {"n_layers": n_layers, "geometry": "llama2-13b (H_kv=40, D=128, bf16)",
+           "compute_stand_in": "bf16 GEMM [T,5120]x[5120,61952] per layer (cuBLAS)",
+           "send_stand_in": "device-to-host copy of each packed layer into pinned memory"}
+    main = torch.cuda.current_stream(dev)
+    for T in prompts:
+        nblk = (T + 15) // 16
+        pool = nblk + 64
+        row = torch.randperm(pool, generator=g)[:nblk].to(torch.int32).to(dev)
+        ks = [randn(pool, 16, H_kv, D) for _ in range(n_layers)]
+        vs = [randn(pool, 16, H_kv, D) for _ in range(n_layers)]
+        X = randn(T, hidden)
+        Y = torch.empty(T, ffn_out, dtype=torch.bfloat16, device=dev)
+        outs = [torch.empty(T, 2, H_kv, D, dtype=torch.bfloat16, device=dev)
+                for _ in range(n_layers)]
+        host = torch.empty(T, 2, H_kv, D, dtype=torch.bfloat16).pin_memory()  # reused
+
+        def send(layer, bufs, stream):
+            with torch.cuda.stream(stream):
+                host.copy_(bufs[0], non_blocking=True)
+
+        lw = tr.LayerwisePack(ks, vs, [row], [T], outs=[[o] for o in outs], send=send)
+
+        def run(mode):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for i in range(n_layers):
+                torch.matmul(X, W, out=Y)
+                if mode == "layer":
+                    lw.layer_done(i, main)
+            if mode == "request":
+                tr.pack_request_level(outs, ks, vs, row, T, stream=main)
+                for i in range(n_layers):
+                    send(i, [outs[i]], main)
+            if mode == "layer":
+                lw.wait(main)
+            b.record(main)
+            return a, b
+
+        times = {}
+        for mode in ("compute", "request", "layer"):
+            run(mode)  # warm-up
+            torch.cuda.synchronize()
+            evs = [run(mode) for _ in range(reps)]
+            torch.cuda.synchronize()
+            times[mode] = float(np.median([x.elapsed_time(y) for x, y in evs]))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(main)
+        tr.pack_request_level(outs, ks, vs, row, T, stream=main)
+        ev[1].record(main)
+        for i in range(n_layers):
+            send(i, [outs[i]], main)
+        ev[2].record(main)
+        torch.cuda.synchronize()
+        t_pack, t_send = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+        layer_bytes = T * 2 * H_kv * D * 2
+        res[f"T={T}"] = {
+            "compute_ms": round(times["compute"], 3),
+            "request_level_ms": round(times["request"], 3),
+            "layer_level_ms": round(times["layer"], 3),
+            "exposed_request_level_ms": round(times["request"] - times["compute"], 3),
+            "exposed_layer_level_ms": round(times["layer"] - times["compute"], 3),
+            "pack_all_layers_ms": round(t_pack, 3),
+            "pack_GBps": round(2 * n_layers * layer_bytes / (t_pack * 1e-3) / 1e9, 1),
+            "send_all_layers_ms": round(t_send, 3),
+            "send_GBps": round(n_layers * layer_bytes / (t_send * 1e-3) / 1e9, 1)}
+        del ks, vs, outs, lw, X, Y, host
+        torch.cuda.empty_cache()
     return res
 
 

@@ -71,6 +71,9 @@ typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2, PDA_NVFP4 = 3 } pda_
 /* Most requests one batched pack or unpack call takes. */
 #define PDA_PACK_MAX_BATCH 64
 
+/* Most layers one pda_kv_pack_layers / pda_kv_unpack_layers call takes. */
+#define PDA_PACK_MAX_LAYERS 256
+
 /* Human-readable name of a status. Never NULL. */
 const char* pda_status_string(pda_status status);
 
@@ -331,6 +334,46 @@ pda_status pda_kv_unpack_blocks_batched(const void* const* ins,
                                         void* v_cache, int H_kv, int D, int block_size,
                                         int num_blocks, pda_dtype kv_dtype, int32_t* error_word,
                                         cudaStream_t stream);
+
+/*
+ * pda_kv_pack_layers -- pda_kv_pack_blocks of one request over n_layers layers' caches, in
+ * one launch.
+ *
+ * A model keeps one K and one V cache per layer, and a request's blocks have the same ids in
+ * every layer (one block table per request). Request-level transfer sends all layers once
+ * prefill ends (page on goodput and PD disaggregation, 0539edu.com, sec. 5.4, request
+ * granularity); layer-level transfer sends layer N as soon as its prefill is done, hidden
+ * behind the computation of the later layers (same page and section, layer granularity;
+ * page "Disaggregated LLM Serving: from PD disaggregation to attention offload", sec. 5.6),
+ * which is one pda_kv_pack_blocks per layer on a transfer stream. This call is the
+ * whole-model form: for layer i < n_layers and t < context_len,
+ *      outs[i][t, 0, :, :] = K of token t in k_caches[i],  outs[i][t, 1, :, :] = V.
+ *
+ *  outs, k_caches, v_caches: HOST arrays of n_layers device pointers, copied into the
+ *                 launch; outs[i] is [context_len, 2, H_kv, D] in kv_dtype, dense; every
+ *                 layer's caches are [num_blocks, block_size, H_kv, D].
+ *  block_table_row device pointer to the request's table row (int32), shared by all layers.
+ *  n_layers <= PDA_PACK_MAX_LAYERS (more: PDA_ERR_UNSUPPORTED); 0 or context_len 0 is a
+ *  no-op. Errors, bitwise copy and alignment as for pda_kv_pack_blocks.
+ */
+pda_status pda_kv_pack_layers(void* const* outs, const void* const* k_caches,
+                              const void* const* v_caches, int n_layers,
+                              const int32_t* block_table_row, int context_len, int H_kv, int D,
+                              int block_size, int num_blocks, pda_dtype kv_dtype,
+                              int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_unpack_layers -- the receiving side of pda_kv_pack_layers: for layer i and
+ * t < context_len, the K row of token t in k_caches[i] = ins[i][t, 0, :, :] and the V row =
+ * ins[i][t, 1, :, :]. HOST arrays of n_layers device pointers, copied into the launch;
+ * semantics per layer as for pda_kv_unpack_blocks (a bad block id sets
+ * PDA_DEVERR_BLOCK_ID and that token is not written in any layer).
+ */
+pda_status pda_kv_unpack_layers(const void* const* ins, void* const* k_caches,
+                                void* const* v_caches, int n_layers,
+                                const int32_t* block_table_row, int context_len, int H_kv,
+                                int D, int block_size, int num_blocks, pda_dtype kv_dtype,
+                                int32_t* error_word, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

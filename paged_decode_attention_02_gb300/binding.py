@@ -20,6 +20,7 @@ from . import build_lib
 PDA_F32, PDA_BF16, PDA_FP8_E4M3, PDA_NVFP4 = 0, 1, 2, 3
 PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PDA_PACK_MAX_BATCH = 64
+PDA_PACK_MAX_LAYERS = 256
 PDA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 EXPORTED = [
@@ -27,7 +28,7 @@ EXPORTED = [
     "pda_attention_workspace_size", "pda_paged_decode_attention", "pda_kv_pack_blocks",
     "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
     "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched", "pda_paged_decode_attention_fp8",
-    "pda_paged_decode_attention_nvfp4",
+    "pda_paged_decode_attention_nvfp4", "pda_kv_pack_layers", "pda_kv_unpack_layers",
 ]
 
 _lock = threading.Lock()
@@ -84,6 +85,12 @@ def load():
         lib.pda_kv_unpack_blocks.restype = I
         lib.pda_kv_unpack_blocks_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P, P]
         lib.pda_kv_unpack_blocks_batched.restype = I
+        # outs/ins, k_caches, v_caches, n_layers, table row, context_len, H_kv, D, bs, NB,
+        # dtype, error_word, stream
+        lib.pda_kv_pack_layers.argtypes = [P, P, P, I, P, I, I, I, I, I, I, P, P]
+        lib.pda_kv_pack_layers.restype = I
+        lib.pda_kv_unpack_layers.argtypes = [P, P, P, I, P, I, I, I, I, I, I, P, P]
+        lib.pda_kv_unpack_layers.restype = I
         _lib = lib
         return lib
 
@@ -331,3 +338,39 @@ def kv_unpack_blocks_batched(packed, k_cache, v_cache, block_table_rows, context
                                                _ptr(v_cache), H_kv, D, bs, NB, _dtype(k_cache),
                                                _ptr(error_word), _stream(stream)),
            "pda_kv_unpack_blocks_batched")
+
+
+def _layer_arrays(bufs, k_caches, v_caches):
+    n = len(bufs)
+    assert len(k_caches) == n and len(v_caches) == n
+    NB, bs, H_kv, D = k_caches[0].shape
+    for k, v in zip(k_caches, v_caches):
+        assert tuple(k.shape) == (NB, bs, H_kv, D) == tuple(v.shape)
+        assert k.dtype == v.dtype == k_caches[0].dtype
+    arr = lambda ts: (ctypes.c_void_p * max(n, 1))(*[_ptr(t).value for t in ts])
+    return n, arr(bufs), arr(k_caches), arr(v_caches), (NB, bs, H_kv, D)
+
+
+def kv_pack_layers(outs, k_caches, v_caches, block_table_row, context_len: int,
+                   error_word=None, stream=None):
+    """One request's blocks in every layer's caches -> ``outs[i]`` ``[context_len, 2, H_kv,
+    D]``, one launch (all layers share the request's block table)."""
+    n, out_arr, k_arr, v_arr, (NB, bs, H_kv, D) = _layer_arrays(outs, k_caches, v_caches)
+    for o in outs:
+        assert o.shape[0] >= context_len and tuple(o.shape[1:]) == (2, H_kv, D)
+    _check(load().pda_kv_pack_layers(out_arr, k_arr, v_arr, n, _ptr(block_table_row),
+                                     int(context_len), H_kv, D, bs, NB, _dtype(k_caches[0]),
+                                     _ptr(error_word), _stream(stream)), "pda_kv_pack_layers")
+    return outs
+
+
+def kv_unpack_layers(packed, k_caches, v_caches, block_table_row, context_len: int,
+                     error_word=None, stream=None):
+    """The inverse of ``kv_pack_layers``: ``packed[i]`` into layer i's caches, one launch."""
+    n, in_arr, k_arr, v_arr, (NB, bs, H_kv, D) = _layer_arrays(packed, k_caches, v_caches)
+    for x in packed:
+        assert x.shape[0] >= context_len and tuple(x.shape[1:]) == (2, H_kv, D)
+    _check(load().pda_kv_unpack_layers(in_arr, k_arr, v_arr, n, _ptr(block_table_row),
+                                       int(context_len), H_kv, D, bs, NB, _dtype(k_caches[0]),
+                                       _ptr(error_word), _stream(stream)),
+           "pda_kv_unpack_layers")

@@ -13,6 +13,10 @@
 //  * unpack: the decode instance receives that buffer and writes it into the blocks it
 //    allocated for the request (same page, sec. 3: the KV is migrated to the decode worker;
 //    page "From PagedAttention to Prefill-Decode disaggregation", sec. 2.2 step 3).
+//  * pack / unpack over layers: one request's blocks in every layer's cache (all layers
+//    share the request's block table) in one launch -- the request-level transfer of a whole
+//    model; layer-by-layer streaming (page on goodput and PD disaggregation, sec. 5.4, layer
+//    granularity; page "Disaggregated LLM Serving", sec. 5.6) issues one layer at a time.
 #include "pda_device.cuh"
 #include "pda_internal.h"
 
@@ -52,15 +56,17 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
 struct PackJob {
   uint4* buf;  // the request's dense [len, 2, H_kv, D] buffer (pack: written, unpack: read)
   const int32_t* table;
+  uint4* k_cache;  // the cache this job reads (pack) or writes (unpack)
+  uint4* v_cache;
   int len;
 };
 
+// N: most jobs one launch carries (kernel parameter space: N * 40 bytes).
+template <int N>
 struct PackParams {
-  uint4* k_cache;
-  uint4* v_cache;
   int32_t* error_word;
   int n, row_vecs, block_size, num_blocks;
-  PackJob jobs[PDA_PACK_MAX_BATCH];
+  PackJob jobs[N];
 };
 
 constexpr int kPackTokens = 4;  // tokens per thread per iteration (loads in flight)
@@ -71,8 +77,8 @@ constexpr int kPackTokens = 4;  // tokens per thread per iteration (loads in fli
 // token (so no per-vector division), for kPackTokens tokens at a time.
 // Pack: a token in a block out of range reads as 0xFF bytes. Unpack: it is not written.
 // Both set PDA_DEVERR_BLOCK_ID.
-template <bool kUnpack>
-__global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ PackParams p) {
+template <bool kUnpack, int N>
+__global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ PackParams<N> p) {
   const PackJob job = p.jobs[blockIdx.y];
   const int rv = p.row_vecs;
   const int row2 = 2 * rv;
@@ -91,7 +97,7 @@ __global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ 
     for (int c = threadIdx.x; c < row2; c += blockDim.x) {
       const bool is_v = c >= rv;
       const int cv = is_v ? c - rv : c;
-      uint4* cache = is_v ? p.v_cache : p.k_cache;
+      uint4* cache = is_v ? job.v_cache : job.k_cache;
       uint4 v[kPackTokens];
 #pragma unroll
       for (int k = 0; k < kPackTokens; ++k) {
@@ -135,7 +141,8 @@ pda_status check_kv_rows(int H_kv, int D, int block_size, int num_blocks, pda_dt
   return PDA_OK;
 }
 
-pda_status launch_blocks(const PackParams& p, int max_len, bool unpack, cudaStream_t stream) {
+template <int N>
+pda_status launch_blocks(const PackParams<N>& p, int max_len, bool unpack, cudaStream_t stream) {
   int gx = (max_len + kPackTokens - 1) / kPackTokens;
   if (gx > 8192) gx = 8192;
   if (gx < 1) gx = 1;
@@ -143,9 +150,9 @@ pda_status launch_blocks(const PackParams& p, int max_len, bool unpack, cudaStre
   // one thread per 16-byte vector of a token's K|V row, at most 256
   const int threads = 2 * p.row_vecs >= 256 ? 256 : (2 * p.row_vecs + 31) / 32 * 32;
   if (unpack)
-    kv_blocks_kernel<true><<<grid, threads, 0, stream>>>(p);
+    kv_blocks_kernel<true, N><<<grid, threads, 0, stream>>>(p);
   else
-    kv_blocks_kernel<false><<<grid, threads, 0, stream>>>(p);
+    kv_blocks_kernel<false, N><<<grid, threads, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
 }
 
@@ -164,9 +171,7 @@ pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_r
       k_cache == nullptr || v_cache == nullptr)
     return PDA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PDA_ERR_INVALID_ARG;
-  PackParams p;
-  p.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
-  p.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+  PackParams<PDA_PACK_MAX_BATCH> p;
   p.error_word = error_word;
   p.row_vecs = rv;
   p.block_size = block_size;
@@ -181,6 +186,8 @@ pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_r
       return PDA_ERR_INVALID_ARG;
     p.jobs[m].buf = static_cast<uint4*>(bufs[i]);
     p.jobs[m].table = block_table_rows[i];
+    p.jobs[m].k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+    p.jobs[m].v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
     p.jobs[m].len = len;
     if (len > max_len) max_len = len;
     ++m;
@@ -190,10 +197,66 @@ pda_status blocks_batched(void* const* bufs, const int32_t* const* block_table_r
   return launch_blocks(p, max_len, unpack, stream);
 }
 
+// Shared front end of the layer calls: one request, one job per layer.
+pda_status blocks_layers(void* const* bufs, void* const* k_caches, void* const* v_caches,
+                         int n_layers, const int32_t* block_table_row, int context_len, int H_kv,
+                         int D, int block_size, int num_blocks, pda_dtype kv_dtype,
+                         int32_t* error_word, bool unpack, cudaStream_t stream) {
+  if (n_layers < 0 || context_len < 0) return PDA_ERR_INVALID_ARG;
+  if (n_layers > PDA_PACK_MAX_LAYERS) return PDA_ERR_UNSUPPORTED;
+  int rv = 0;
+  const pda_status st = check_kv_rows(H_kv, D, block_size, num_blocks, kv_dtype, &rv);
+  if (st != PDA_OK) return st;
+  if (n_layers == 0 || context_len == 0) return PDA_OK;
+  if (bufs == nullptr || k_caches == nullptr || v_caches == nullptr ||
+      block_table_row == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  PackParams<PDA_PACK_MAX_LAYERS> p;
+  p.error_word = error_word;
+  p.row_vecs = rv;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.n = n_layers;
+  for (int i = 0; i < n_layers; ++i) {
+    if (bufs[i] == nullptr || k_caches[i] == nullptr || v_caches[i] == nullptr ||
+        !aligned16(bufs[i]) || !aligned16(k_caches[i]) || !aligned16(v_caches[i]))
+      return PDA_ERR_INVALID_ARG;
+    p.jobs[i].buf = static_cast<uint4*>(bufs[i]);
+    p.jobs[i].table = block_table_row;
+    p.jobs[i].k_cache = static_cast<uint4*>(k_caches[i]);
+    p.jobs[i].v_cache = static_cast<uint4*>(v_caches[i]);
+    p.jobs[i].len = context_len;
+  }
+  return launch_blocks(p, context_len, unpack, stream);
+}
+
 }  // namespace
 }  // namespace pda
 
 using namespace pda;
+
+extern "C" pda_status pda_kv_pack_layers(void* const* outs, const void* const* k_caches,
+                                         const void* const* v_caches, int n_layers,
+                                         const int32_t* block_table_row, int context_len,
+                                         int H_kv, int D, int block_size, int num_blocks,
+                                         pda_dtype kv_dtype, int32_t* error_word,
+                                         cudaStream_t stream) {
+  return blocks_layers(outs, const_cast<void* const*>(k_caches),
+                       const_cast<void* const*>(v_caches), n_layers, block_table_row,
+                       context_len, H_kv, D, block_size, num_blocks, kv_dtype, error_word, false,
+                       stream);
+}
+
+extern "C" pda_status pda_kv_unpack_layers(const void* const* ins, void* const* k_caches,
+                                           void* const* v_caches, int n_layers,
+                                           const int32_t* block_table_row, int context_len,
+                                           int H_kv, int D, int block_size, int num_blocks,
+                                           pda_dtype kv_dtype, int32_t* error_word,
+                                           cudaStream_t stream) {
+  return blocks_layers(const_cast<void* const*>(ins), k_caches, v_caches, n_layers,
+                       block_table_row, context_len, H_kv, D, block_size, num_blocks, kv_dtype,
+                       error_word, true, stream);
+}
 
 extern "C" pda_status pda_kv_append(const void* k_new, const void* v_new, void* k_cache,
                                     void* v_cache, const int32_t* slot_mapping, int B, int H_kv,
