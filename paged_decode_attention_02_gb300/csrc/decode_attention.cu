@@ -66,9 +66,23 @@ constexpr int kMaxWarps = PDA_ATTN_WARPS > PDA_TC_WARPS ? PDA_ATTN_WARPS : PDA_T
 __host__ __device__ constexpr int warps_for_group(int G, bool tc) {
   return tc ? PDA_TC_WARPS : (G >= 8 ? 8 : PDA_ATTN_WARPS);
 }
+// The two-head tensor-core step holds both heads' q fragments and running state (about 230
+// registers). A scheduler's register file (16K) holds three warps only below 171 registers
+// each, so this step runs 8 warps (two per scheduler), each moving two heads per step.
+#ifndef PDA_TC_PAIR_WARPS
+#define PDA_TC_PAIR_WARPS 8
+#endif
+__host__ __device__ constexpr int warps_for_mode(int G, int mode) {
+  return mode == 2 ? PDA_TC_PAIR_WARPS : warps_for_group(G, mode != 0);
+}
 // Stage alignment: the tensor-core step reads TMA tiles written with the 128-byte (FP8) or
 // 64-byte (NVFP4) swizzle, whose pattern repeats every 1024 (512) bytes.
 __host__ __device__ constexpr int stage_align(bool tc) { return tc ? 1024 : 128; }
+
+// Tile steps (see attn_partial_kernel).
+constexpr int kModeCuda = 0;
+constexpr int kModeTc = 1;
+constexpr int kModeTcPair = 2;
 constexpr int kMetaBytesPerWarp = 2 * 32 * 8;  // two groups of 32 (block id, length) pairs
 constexpr int kMaxBatch = 8192;     // prefix table size bound (shared memory)
 constexpr int kSmemBudget = 226 * 1024;  // dynamic bytes; static shared memory sits on top
@@ -516,14 +530,24 @@ __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1,
     merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, W_tiles, NW, lane);
 }
 
-// TC selects the tile step: the tensor-core one (quantised caches, D = 128) or the
-// CUDA-core one.
-template <typename KV, typename QT, int D, int G, bool TC>
-__global__ void __launch_bounds__(warps_for_group(G, TC) * 32, 1)
+// MODE selects the tile step: kModeCuda (CUDA cores), kModeTc (tensor cores, one kv-head
+// per tile) or kModeTcPair (tensor cores, two adjacent kv-heads per tile, loaded by one
+// 4-D TMA box). G is the unit's query heads: the kv-head's G, or 2 G for a pair; p.H_kv
+// counts units (kv-heads, or pairs).
+template <typename KV, typename QT, int D, int G, int MODE>
+__global__ void __launch_bounds__(warps_for_mode(G, MODE) * 32, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  constexpr bool TC = MODE != kModeCuda;
   using Geo = Geometry<KV, QT, D, G>;
-  using W = std::conditional_t<TC, WarpAttnTC<KV, D, G>, WarpAttn<KV, QT, D, G>>;
+  using W = std::conditional_t<
+      MODE == kModeCuda, WarpAttn<KV, QT, D, G>,
+      std::conditional_t<MODE == kModeTc, WarpAttnTC<KV, D, G>, WarpAttnTCPair<KV, D, G / 2>>>;
+  // a unit's tile: one head tile, or a pair's two head tiles back to back
+  constexpr int kHeads = MODE == kModeTcPair ? 2 : 1;
+  constexpr uint32_t kTile = kHeads * Geo::TILE_BYTES;
+  constexpr uint32_t kScales = kHeads * Geo::SCALE_BYTES;
+  constexpr int kRowScales = kHeads * Geo::ROW_SCALES;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // The host reserves stage_align(TC) - 128 spare bytes; the layout starts at the first
   // aligned address (swizzled TMA tiles need the swizzle period's alignment).
@@ -621,18 +645,16 @@ __global__ void __launch_bounds__(warps_for_group(G, TC) * 32, 1)
   int32_t* my_info = s_info + warp * p.stages;
   auto k_buf = [&](int s) { return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes); };
   auto v_buf = [&](int s) {
-    return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + Geo::TILE_BYTES);
+    return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + kTile);
   };
   auto ks_buf = [&](int s) {  // NVFP4 block scales of the K tile, [16][D/16]
-    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES);
+    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * kTile);
   };
   auto vs_buf = [&](int s) {
-    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES +
-                                      Geo::SCALE_BYTES);
+    return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * kTile + kScales);
   };
   auto q_buf = [&](int s) {
-    return reinterpret_cast<QT*>(my_stage + s * p.stage_bytes + 2 * Geo::TILE_BYTES +
-                                 2 * Geo::SCALE_BYTES);
+    return reinterpret_cast<QT*>(my_stage + s * p.stage_bytes + 2 * kTile + 2 * kScales);
   };
 
   // (request, kv-head, block) of tile y
@@ -700,9 +722,9 @@ __global__ void __launch_bounds__(warps_for_group(G, TC) * 32, 1)
       const int r = lane & 15;
       const bool is_v = lane >= 16;
       const uint8_t* src = (is_v ? p.v_bscales : p.k_bscales) +
-                           ((static_cast<size_t>(pid) * kBS + r) * H_kv + h) * Geo::ROW_SCALES;
-      uint8_t* dst = (is_v ? vs_buf(s) : ks_buf(s)) + r * Geo::ROW_SCALES;
-      cp_async_n<Geo::ROW_SCALES>(dst, src);
+                           ((static_cast<size_t>(pid) * kBS + r) * H_kv + h) * kRowScales;
+      uint8_t* dst = (is_v ? vs_buf(s) : ks_buf(s)) + r * kRowScales;
+      cp_async_n<kRowScales>(dst, src);
       cp_async_mbar_arrive_noinc(&my_bar[s]);
     }
     if (lane == x - g_base) {
@@ -711,11 +733,16 @@ __global__ void __launch_bounds__(warps_for_group(G, TC) * 32, 1)
       const int n_valid = min(kBS, cur_len - cur_blk * kBS);
       my_info[s] = n_valid | (bad ? 0x100 : 0);
       if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
-      const uint32_t bytes = 2 * Geo::TILE_BYTES + (need_q ? Geo::Q_BYTES : 0);
+      const uint32_t bytes = 2 * kTile + (need_q ? Geo::Q_BYTES : 0);
       mbar_arrive_expect_tx(&my_bar[s], bytes);
       const int row = (bad ? 0 : cur_pid) * kBS;
-      tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
-      tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
+      if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
+        tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
+        tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);
+      } else {
+        tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
+        tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
+      }
       if (need_q) {
         const QT* src = reinterpret_cast<const QT*>(p.q) +
                         (static_cast<size_t>(cur_b) * p.H + static_cast<size_t>(cur_h) * G) * D;
@@ -858,34 +885,49 @@ size_t q_bytes_for(pda_dtype kv) {
   return (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4) ? 2u : dtype_bytes(kv);
 }
 
-// Quantised caches at D = 128 with G >= 2 query heads per kv-head take the tensor-core tile
-// step. With G = 1 the tile is a plain GEMV (one dot product per K element) and the CUDA
-// cores keep up with HBM: measured equal for FP8 and 3 % faster for NVFP4 on llama2-13b
-// shapes, while at G = 4 the tensor cores are 1.5x faster.
-bool use_tc(pda_dtype kv, int D, int G) {
-  return (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4) && D == 128 && G >= 2;
+// How a launch tiles the work: the tile step and the unit (one kv-head, or a pair).
+struct Tiling {
+  int mode;   // kModeCuda, kModeTc or kModeTcPair
+  int H_u;    // units per request (kv-heads, or pairs)
+  int G_u;    // query heads per unit
+};
+
+// Quantised caches at D = 128 run on the tensor cores. Where H_kv is even and G <= 4, two
+// adjacent kv-heads share a tile (one TMA box and one pipeline step for both): per byte
+// that halves the TMA operations, which bound small quantised tiles (about one per 120 SM
+// cycles, whatever their size), and the per-tile pipeline work. Otherwise a quantised tile
+// is one kv-head on the tensor cores for G >= 2, and on the CUDA cores for G = 1 (a plain
+// GEMV, where they keep up: measured equal to the single-head tensor-core step).
+Tiling tiling_for(pda_dtype kv, int D, int H_kv, int G) {
+  const bool quantised = kv == PDA_FP8_E4M3 || kv == PDA_NVFP4;
+  if (quantised && D == 128 && G <= 4 && H_kv % 2 == 0) return {kModeTcPair, H_kv / 2, 2 * G};
+  if (quantised && D == 128 && G >= 2) return {kModeTc, H_kv, G};
+  return {kModeCuda, H_kv, G};
 }
 
-// One pipeline stage: the K and V tiles, (NVFP4) their block scales, the q rows.
-uint32_t stage_bytes_for(pda_dtype kv, int D, int G) {
-  const size_t tile = kv == PDA_NVFP4 ? kBS * D / 2 : kBS * D * dtype_bytes(kv);
-  const size_t scales = kv == PDA_NVFP4 ? 2 * kBS * D / 16 : 0;
-  const size_t q = static_cast<size_t>(G) * D * q_bytes_for(kv);
-  return static_cast<uint32_t>(round_up(2 * tile + scales + q, stage_align(use_tc(kv, D, G))));
+// One pipeline stage: the K and V tiles, (NVFP4) their block scales, the q rows, for a unit.
+uint32_t stage_bytes_for(pda_dtype kv, int D, const Tiling& t) {
+  const size_t heads = t.mode == kModeTcPair ? 2 : 1;
+  const size_t tile = heads * (kv == PDA_NVFP4 ? kBS * D / 2 : kBS * D * dtype_bytes(kv));
+  const size_t scales = heads * (kv == PDA_NVFP4 ? 2 * kBS * D / 16 : 0);
+  const size_t q = static_cast<size_t>(t.G_u) * D * q_bytes_for(kv);
+  return static_cast<uint32_t>(
+      round_up(2 * tile + scales + q, stage_align(t.mode != kModeCuda)));
 }
 
 bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
                LaunchPlan* pl) {
-  const bool tc = use_tc(kv, D, G);
+  const Tiling t = tiling_for(kv, D, H_kv, G);
+  const bool tc = t.mode != kModeCuda;
   const size_t align = stage_align(tc);
-  pl->stage_bytes = stage_bytes_for(kv, D, G);
+  pl->stage_bytes = stage_bytes_for(kv, D, t);
   pl->prefix_bytes = static_cast<uint32_t>(round_up(static_cast<size_t>(B + 1) * 4, align));
   // + alignment of the metadata ring, + room to align the layout's start
   const size_t fixed = pl->prefix_bytes + 8 + (align - 128);
   if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
   pl->nwarps = 0;
   // The most warps that still get two stages each; then as many stages as fit.
-  for (int nw = warps_for_group(G, tc); nw >= 2; --nw) {
+  for (int nw = warps_for_mode(t.G_u, t.mode); nw >= 2; --nw) {
     const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
     const size_t meta = static_cast<size_t>(nw) * kMetaBytesPerWarp;
     if (fixed + meta >= static_cast<size_t>(kSmemBudget)) continue;
@@ -907,38 +949,60 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
   pl->grid = grid;
   const size_t nw_total = static_cast<size_t>(grid) * pl->nwarps;
   pl->ws_arrive = 0;
-  pl->ws_ml = round_up(static_cast<size_t>(B) * H_kv * 8, 256);
-  pl->ws_o = pl->ws_ml + round_up(2 * nw_total * G * 2 * 4, 256);
-  pl->ws_total = pl->ws_o + round_up(2 * nw_total * G * static_cast<size_t>(D) * 4, 256);
+  pl->ws_ml = round_up(static_cast<size_t>(B) * t.H_u * 8, 256);
+  pl->ws_o = pl->ws_ml + round_up(2 * nw_total * t.G_u * 2 * 4, 256);
+  pl->ws_total = pl->ws_o + round_up(2 * nw_total * t.G_u * static_cast<size_t>(D) * 4, 256);
   return true;
 }
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnParams);
 
-template <typename KV, typename QT, int D, bool TC = false>
-KernelFn pick_g(int G) {
-  switch (G) {
-    case 1: return attn_partial_kernel<KV, QT, D, 1, false>;  // see use_tc
-    case 2: return attn_partial_kernel<KV, QT, D, 2, TC>;
-    case 4: return attn_partial_kernel<KV, QT, D, 4, TC>;
-    case 8: return attn_partial_kernel<KV, QT, D, 8, TC>;
+// The kernel for a unit of G_u query heads in the given mode.
+template <typename KV, typename QT, int D>
+KernelFn pick_g(int G_u, int mode) {
+  if constexpr (std::is_same<KV, fp8e4m3>::value || std::is_same<KV, nvfp4>::value) {
+    if constexpr (D == 128) {
+      if (mode == kModeTcPair) {
+        switch (G_u) {
+          case 2: return attn_partial_kernel<KV, QT, D, 2, kModeTcPair>;
+          case 4: return attn_partial_kernel<KV, QT, D, 4, kModeTcPair>;
+          case 8: return attn_partial_kernel<KV, QT, D, 8, kModeTcPair>;
+          default: return nullptr;
+        }
+      }
+      if (mode == kModeTc) {
+        switch (G_u) {
+          case 2: return attn_partial_kernel<KV, QT, D, 2, kModeTc>;
+          case 4: return attn_partial_kernel<KV, QT, D, 4, kModeTc>;
+          case 8: return attn_partial_kernel<KV, QT, D, 8, kModeTc>;
+          default: return nullptr;
+        }
+      }
+    }
+  }
+  if (mode != kModeCuda) return nullptr;
+  switch (G_u) {
+    case 1: return attn_partial_kernel<KV, QT, D, 1, kModeCuda>;
+    case 2: return attn_partial_kernel<KV, QT, D, 2, kModeCuda>;
+    case 4: return attn_partial_kernel<KV, QT, D, 4, kModeCuda>;
+    case 8: return attn_partial_kernel<KV, QT, D, 8, kModeCuda>;
     default: return nullptr;
   }
 }
 
-KernelFn pick_kernel(pda_dtype kv, int D, int G) {
+KernelFn pick_kernel(pda_dtype kv, int D, const Tiling& t) {
   if (kv == PDA_BF16) {
-    if (D == 128) return pick_g<__nv_bfloat16, __nv_bfloat16, 128>(G);
-    if (D == 64) return pick_g<__nv_bfloat16, __nv_bfloat16, 64>(G);
+    if (D == 128) return pick_g<__nv_bfloat16, __nv_bfloat16, 128>(t.G_u, t.mode);
+    if (D == 64) return pick_g<__nv_bfloat16, __nv_bfloat16, 64>(t.G_u, t.mode);
   } else if (kv == PDA_FP8_E4M3) {
-    if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128, true>(G);
-    if (D == 64) return pick_g<fp8e4m3, __nv_bfloat16, 64>(G);
+    if (D == 128) return pick_g<fp8e4m3, __nv_bfloat16, 128>(t.G_u, t.mode);
+    if (D == 64) return pick_g<fp8e4m3, __nv_bfloat16, 64>(t.G_u, t.mode);
   } else if (kv == PDA_NVFP4) {
-    if (D == 128) return pick_g<nvfp4, __nv_bfloat16, 128, true>(G);
-    if (D == 64) return pick_g<nvfp4, __nv_bfloat16, 64>(G);
+    if (D == 128) return pick_g<nvfp4, __nv_bfloat16, 128>(t.G_u, t.mode);
+    if (D == 64) return pick_g<nvfp4, __nv_bfloat16, 64>(t.G_u, t.mode);
   } else {
-    if (D == 128) return pick_g<float, float, 128>(G);
-    if (D == 64) return pick_g<float, float, 64>(G);
+    if (D == 128) return pick_g<float, float, 128>(t.G_u, t.mode);
+    if (D == 64) return pick_g<float, float, 64>(t.G_u, t.mode);
   }
   return nullptr;
 }
@@ -968,9 +1032,11 @@ pda_status allow_max_smem(const void* fn, int dev) {
 struct MapKey {
   const void* base;
   int num_blocks, block_size, H_kv, D, dtype, swizzle;
+  bool pair;
   bool operator==(const MapKey& o) const {
     return base == o.base && num_blocks == o.num_blocks && block_size == o.block_size &&
-           H_kv == o.H_kv && D == o.D && dtype == o.dtype && swizzle == o.swizzle;
+           H_kv == o.H_kv && D == o.D && dtype == o.dtype && swizzle == o.swizzle &&
+           pair == o.pair;
   }
 };
 constexpr int kMapCache = 8;
@@ -979,11 +1045,12 @@ MapKey g_map_key[kMapCache];
 CUtensorMap g_map_val[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
+// pair: the two-head map of encode_kv_pair_tensor_map (byte caches; D = row bytes).
 pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
                                 int block_size, int H_kv, int D, pda_dtype dtype,
-                                int swizzle_bytes) {
+                                int swizzle_bytes, bool pair) {
   const MapKey key{base, num_blocks, block_size, H_kv, D, static_cast<int>(dtype),
-                   swizzle_bytes};
+                   swizzle_bytes, pair};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_map_used; ++i)
@@ -993,7 +1060,9 @@ pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
       }
   }
   const pda_status st =
-      encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype, swizzle_bytes);
+      pair ? encode_kv_pair_tensor_map(tm, base, num_blocks, block_size, H_kv, D, swizzle_bytes)
+           : encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype,
+                                  swizzle_bytes);
   if (st != PDA_OK) return st;
   std::lock_guard<std::mutex> lock(g_map_mu);
   g_map_key[g_map_next] = key;
@@ -1074,7 +1143,8 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   if (!make_plan(B, H_kv, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
   if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
 
-  KernelFn fn = pick_kernel(kv_dtype, D, G);
+  const Tiling tiling = tiling_for(kv_dtype, D, H_kv, G);
+  KernelFn fn = pick_kernel(kv_dtype, D, tiling);
   if (fn == nullptr) return PDA_ERR_UNSUPPORTED;
   st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
   if (st != PDA_OK) return st;
@@ -1083,13 +1153,14 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   // swizzle span is one whole row (128 bytes FP8, 64 bytes NVFP4)
   const int row_elems = kv_dtype == PDA_NVFP4 ? D / 2 : D;
   const pda_dtype map_type = kv_dtype == PDA_NVFP4 ? PDA_FP8_E4M3 : kv_dtype;
-  const int swizzle = use_tc(kv_dtype, D, G) ? row_elems : 0;
+  const int swizzle = tiling.mode != kModeCuda ? row_elems : 0;
+  const bool pair = tiling.mode == kModeTcPair;
   CUtensorMap tmK, tmV;
   st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, row_elems, map_type,
-                            swizzle);
+                            swizzle, pair);
   if (st != PDA_OK) return st;
   st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, row_elems, map_type,
-                            swizzle);
+                            swizzle, pair);
   if (st != PDA_OK) return st;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -1108,7 +1179,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.v_bscales = static_cast<const uint8_t*>(v_bscales);
   ap.B = B;
   ap.H = H;
-  ap.H_kv = H_kv;
+  ap.H_kv = tiling.H_u;  // units: kv-heads, or pairs of them
   ap.num_blocks = num_blocks;
   ap.max_blocks = max_blocks_per_seq;
   ap.max_context_len = max_context_len;

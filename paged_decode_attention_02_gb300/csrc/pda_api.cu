@@ -84,6 +84,37 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
   return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
 }
 
+
+pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
+                                     int block_size, int H_kv, int row_bytes,
+                                     int swizzle_bytes) {
+  std::call_once(g_encode_once, load_encoder);
+  if (g_encode == nullptr) return PDA_ERR_CUDA;
+  if (H_kv % 2 != 0 || (swizzle_bytes != 0 && swizzle_bytes != row_bytes) ||
+      (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128))
+    return PDA_ERR_INVALID_ARG;
+  const cuuint64_t X = static_cast<cuuint64_t>(row_bytes);
+  // dims, innermost first: a row's bytes, the cache rows, the two heads of a pair, the pairs
+  const cuuint64_t dims[4] = {X, static_cast<cuuint64_t>(num_blocks) * block_size, 2,
+                              static_cast<cuuint64_t>(H_kv / 2)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H_kv) * X, X, 2 * X};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(X), static_cast<cuuint32_t>(block_size),
+                             2u, 1u};
+  const cuuint32_t elem_strides[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
+  // both heads of a pair are used, so the fill may cover the pair's 2 * row_bytes
+  const cuuint64_t pair = 2 * X;
+  const CUtensorMapL2promotion promo = pair >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : pair >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                     : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base),
+                              dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
+}
+
 }  // namespace pda
 
 extern "C" const char* pda_status_string(pda_status status) {

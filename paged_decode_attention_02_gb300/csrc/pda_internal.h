@@ -21,6 +21,15 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
                                 int block_size, int H_kv, int D, pda_dtype dtype,
                                 int swizzle_bytes);
 
+// A 4-D tiled tensor map over a byte cache [num_blocks * block_size, H_kv, row_bytes] that
+// loads the tiles of two adjacent kv-heads (2h', 2h' + 1) with one box: dims {row_bytes,
+// rows, 2, H_kv / 2}, box {row_bytes, block_size, 1 pair}; in shared memory the box is head
+// 2h''s block_size rows followed by head 2h' + 1's, each row swizzled as by
+// encode_kv_tensor_map. H_kv must be even.
+pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
+                                     int block_size, int H_kv, int row_bytes,
+                                     int swizzle_bytes);
+
 inline size_t dtype_bytes(pda_dtype t) {
   return t == PDA_BF16 ? 2u : (t == PDA_FP8_E4M3 ? 1u : 4u);
 }

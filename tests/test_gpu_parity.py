@@ -418,8 +418,11 @@ def test_unpack_bad_block_is_skipped_with_error_bit():
 
 
 # ------------------------------------------------------------------ FP8 E4M3 KV cache
-FP8_SHAPES = [(128, 32, 32), (128, 32, 16), (128, 32, 8), (128, 32, 4), (64, 16, 16),
-              (64, 16, 4)]
+# D = 128: kv-head pairs on the tensor cores for G <= 4 and even H_kv (32/32, 32/16, 32/8),
+# one kv-head per tile on the tensor cores for G = 8 (32/4) or odd H_kv with G >= 2 (12/3,
+# 6/3), CUDA cores for odd H_kv with G = 1 (5/5); D = 64: CUDA cores.
+FP8_SHAPES = [(128, 32, 32), (128, 32, 16), (128, 32, 8), (128, 32, 4), (128, 12, 3),
+              (128, 6, 3), (128, 5, 5), (64, 16, 16), (64, 16, 4)]
 
 
 @pytest.mark.parametrize("D,H,H_kv", FP8_SHAPES)
@@ -486,8 +489,8 @@ def test_fp8_entry_rejects_plain_caches_and_base_entry_rejects_fp8():
 
 
 # ------------------------------------------------------------------ NVFP4 KV cache
-NVFP4_SHAPES = [(128, 32, 32), (128, 32, 8), (128, 16, 2), (128, 64, 8), (64, 16, 4),
-                (64, 16, 16)]
+NVFP4_SHAPES = [(128, 32, 32), (128, 32, 8), (128, 32, 16), (128, 16, 2), (128, 64, 8),
+                (128, 12, 3), (128, 5, 5), (64, 16, 4), (64, 16, 16)]
 
 
 @pytest.mark.parametrize("D,H,H_kv", NVFP4_SHAPES)
@@ -495,9 +498,12 @@ def test_nvfp4_shapes_and_groups(D, H, H_kv):
     w = variant("llama2_13b_b80_nvfp4", D=D, H=H, H_kv=H_kv, B=9, lengths="uniform:1,700")
     lens = np.array([1, 15, 16, 17, 31, 32, 33, 700, 255], np.int32)
     s = wl.make_step(w, device=DEV, lengths=lens)
-    ref, st, kc, vc = oracle_full_step(s)
+    # the byte append needs 16-byte rows: H_kv * D / 16 scale bytes (odd H_kv at D = 128
+    # gives 8-byte multiples), so those shapes test the attention alone
+    append = (H_kv * D // 16) % 16 == 0
+    ref, st, kc, vc = oracle_full_step(s, append=append)
     assert st == 0
-    out, err = gpu_step(s)
+    out, err = gpu_step(s, append=append)
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
     assert_attention_close(out, ref, f"nvfp4 D={D} H={H} H_kv={H_kv}")
@@ -589,7 +595,7 @@ def test_tc_sharp_softmax_rescales(name, boost):
 
 
 @pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
-@pytest.mark.parametrize("H,H_kv", [(64, 8), (16, 8), (8, 8)])
+@pytest.mark.parametrize("H,H_kv", [(64, 8), (16, 8), (8, 8), (12, 3), (7, 7)])
 def test_tc_groups_with_ragged_tails(kv, H, H_kv):
     """Group sizes 8 and 2 (tensor cores) and 1 (CUDA cores), lengths that end at every
     offset of a block (partial tiles mask tokens 1..15 of the last block)."""
