@@ -68,12 +68,20 @@ __host__ __device__ constexpr int warps_for_group(int G, bool tc) {
 }
 // The two-head tensor-core step holds both heads' q fragments and running state (about 230
 // registers). A scheduler's register file (16K) holds three warps only below 171 registers
-// each, so this step runs 8 warps (two per scheduler), each moving two heads per step.
-#ifndef PDA_TC_PAIR_WARPS
-#define PDA_TC_PAIR_WARPS 8
+// each. FP8 runs it with 8 warps (two per scheduler, no spills); NVFP4, whose longer
+// dequantisation chains need more warps to hide, with 12 and a few spilled registers
+// (measured 9-10 % faster for NVFP4 and 2 % slower for FP8 than the other choice).
+#ifndef PDA_TC_PAIR_WARPS_FP8
+#define PDA_TC_PAIR_WARPS_FP8 8
 #endif
-__host__ __device__ constexpr int warps_for_mode(int G, int mode) {
-  return mode == 2 ? PDA_TC_PAIR_WARPS : warps_for_group(G, mode != 0);
+#ifndef PDA_TC_PAIR_WARPS_NVFP4
+#define PDA_TC_PAIR_WARPS_NVFP4 12
+#endif
+static_assert(PDA_TC_PAIR_WARPS_FP8 <= kMaxWarps && PDA_TC_PAIR_WARPS_NVFP4 <= kMaxWarps,
+              "per-warp shared arrays are sized for kMaxWarps");
+__host__ __device__ constexpr int warps_for_mode(int G, int mode, bool fp4) {
+  return mode == 2 ? (fp4 ? PDA_TC_PAIR_WARPS_NVFP4 : PDA_TC_PAIR_WARPS_FP8)
+                   : warps_for_group(G, mode != 0);
 }
 // Stage alignment: the tensor-core step reads TMA tiles written with the 128-byte (FP8) or
 // 64-byte (NVFP4) swizzle, whose pattern repeats every 1024 (512) bytes.
@@ -535,7 +543,8 @@ __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1,
 // 4-D TMA box). G is the unit's query heads: the kv-head's G, or 2 G for a pair; p.H_kv
 // counts units (kv-heads, or pairs).
 template <typename KV, typename QT, int D, int G, int MODE>
-__global__ void __launch_bounds__(warps_for_mode(G, MODE) * 32, 1)
+__global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4>::value) * 32,
+                                  1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   constexpr bool TC = MODE != kModeCuda;
@@ -927,7 +936,7 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
   if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
   pl->nwarps = 0;
   // The most warps that still get two stages each; then as many stages as fit.
-  for (int nw = warps_for_mode(t.G_u, t.mode); nw >= 2; --nw) {
+  for (int nw = warps_for_mode(t.G_u, t.mode, kv == PDA_NVFP4); nw >= 2; --nw) {
     const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
     const size_t meta = static_cast<size_t>(nw) * kMetaBytesPerWarp;
     if (fixed + meta >= static_cast<size_t>(kSmemBudget)) continue;
