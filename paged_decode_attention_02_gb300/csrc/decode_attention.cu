@@ -496,19 +496,34 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
       }
     }
     const int n = min(32, w1 - base + 1);
-    for (int i = 0; i < n; ++i) {
-      if (!live(base + i)) continue;
-      const float* row = p.ws_o + (static_cast<size_t>(slot_of(base + i)) * G + j0) * D;
-      float v[HP][PER];
+    // U pieces' rows in flight at once (each load is an L2 round trip). A dead or missing
+    // piece reads piece w0's row (always written: w0 holds the segment's first tile) and is
+    // left out of the sum by its flag, not by a zero weight (its row may hold NaN).
+    constexpr int U = HP * PER <= 4 ? 4 : 1;  // wider would spill in the kernels with G >= 2
+    for (int i0 = 0; i0 < n; i0 += U) {
+      float v[U][HP][PER];
+      float fu[U][HP];
+      bool use[U];
 #pragma unroll
-      for (int j = 0; j < HP; ++j)
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u;
+        use[u] = i < n && live(base + i);
+        const float* row =
+            p.ws_o + (static_cast<size_t>(slot_of(use[u] ? base + i : w0)) * G + j0) * D;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) v[j][e] = __ldcg(row + j * D + lane + 32 * e);
+        for (int j = 0; j < HP; ++j) {
+          fu[u][j] = __shfl_sync(kFullMask, f[j], i < n ? i : 0);
 #pragma unroll
-      for (int j = 0; j < HP; ++j) {
-        const float fi = __shfl_sync(kFullMask, f[j], i);
+          for (int e = 0; e < PER; ++e) v[u][j][e] = __ldcg(row + j * D + lane + 32 * e);
+        }
+      }
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[j][e] = fmaf(v[j][e], fi, acc[j][e]);
+      for (int u = 0; u < U; ++u) {
+        if (!use[u]) continue;
+#pragma unroll
+        for (int j = 0; j < HP; ++j)
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[j][e] = fmaf(v[u][j][e], fu[u][j], acc[j][e]);
       }
     }
   }
