@@ -608,3 +608,49 @@ def test_tc_groups_with_ragged_tails(kv, H, H_kv):
     out, err = gpu_step(s, append=False)
     assert err == 0
     assert_attention_close(out, ref, f"{kv} H={H} H_kv={H_kv} ragged")
+
+
+# ------------------------------------------------------------------ quantised edge cases
+# The two-kv-head tiles (every quantised workload) go through the same scheduling, merge
+# and error paths as the bf16 kernel with units of two kv-heads and 2G query heads.
+@pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "gqa_skew_b256_nvfp4",
+                                  "llama2_13b_b80_nvfp4"])
+@pytest.mark.parametrize("cap", [1, 7, 61, 152])
+def test_quantised_sm_cap_does_not_change_results(name, cap):
+    s = wl.make_step(name, device=DEV, B=10)
+    ref, _, _, _ = oracle_full_step(s, append=False)
+    out, err = gpu_step(s, append=False, sm_cap=cap)
+    assert err == 0
+    assert_attention_close(out, ref, f"{name} sm_cap={cap}")
+
+
+@pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4"])
+def test_quantised_repeat_runs_are_bitwise_identical(name):
+    s = wl.make_step(name, device=DEV, B=24)
+    a, _ = gpu_step(s, append=False)
+    b, _ = gpu_step(s, append=False)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "gqa_skew_b256_nvfp4"])
+def test_quantised_bad_block_id_gives_nan_rows_and_error_bit(name):
+    lens = np.array([40, 40, 40], np.int32)
+    s = wl.make_step(variant(name, B=3), device=DEV, lengths=lens)
+    s.block_tables[1, 1] = s.num_blocks + 7
+    out, err = gpu_step(s, append=False)
+    assert err & binding.PDA_DEVERR_BLOCK_ID
+    assert torch.isnan(out[1].float()).all()
+    assert torch.isfinite(out[0].float()).all() and torch.isfinite(out[2].float()).all()
+
+
+@pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4"])
+def test_quantised_single_very_long_request_split_over_every_worker(name):
+    """One 20000-token request: every kv-head pair's segment is cut over many workers and
+    merged (2G heads per unit)."""
+    lens = np.array([20000], np.int32)
+    s = wl.make_step(variant(name, B=1, lengths="uniform:1,20000"), device=DEV, lengths=lens)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0
+    out, err = gpu_step(s, append=False)
+    assert err == 0
+    assert_attention_close(out, ref, f"{name} one long request")
