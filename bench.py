@@ -405,39 +405,62 @@ def run_ours(args, ws, rank, local):
     t_step = np.mean([e[0].elapsed_time(e[3]) for e in evs]) * 1e-3
     t_step_max = dist_max(t_step, ws)
 
-    # ---- end to end: per-step inputs from pinned host memory, results back to host
+    # ---- end to end: per-step inputs from pinned host memory, results back to host.
+    # A serving loop overlaps the copy-out of step k (attention output and packed KV, about
+    # 1 GB, bound by the ~190 GB/s device-to-host link) with the compute of step k + 1: two
+    # sets of output buffers, the copies on their own stream; step k waits only for the
+    # copy-out that last used its buffer set. Timed over the whole loop (inputs larger than
+    # L2, so no flush inside it).
     d_in = [s.q] + [t for _, _, kn, vn in arrays for t in (kn, vn)] + [
         s.slot_mapping, s.block_tables, s.context_lens]
     h_in = [x.detach().cpu().pin_memory() for x in d_in]
-    h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory()] + [
-        torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in packs]
-    d_out = [out] + packs
+    outs2 = [out, torch.empty_like(out)]
+    packs2 = [packs_of, [[torch.empty_like(p) for p in group] for group in packs_of]]
+    h_out2 = [[torch.empty(out.shape, dtype=out.dtype).pin_memory()] + [
+        torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in packs] for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    d2h = sum(x.numel() * x.element_size() for x in h_out2[0])
+    copy_stream = torch.cuda.Stream(dev)
+    computed = [torch.cuda.Event() for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    for e in copied:
+        e.record(stream)
 
-    def e2e_step():
+    def e2e_step(k):
+        b = k % 2
+        stream.wait_event(copied[b])  # buffer set b is free again
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        step()
-        for d, h in zip(d_out, h_out):
-            h.copy_(d, non_blocking=True)
+        for kc, vc, kn, vn in arrays:
+            pda.kv_append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
+        attention(s, outs2[b], cap, wsp, error_word=err)
+        if pack_reqs:
+            for (kc, vc, _, _), group in zip(arrays, packs2[b]):
+                pda.kv_pack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
+                                           error_word=err)
+        computed[b].record(stream)
+        copy_stream.wait_event(computed[b])
+        with torch.cuda.stream(copy_stream):
+            d_out = [outs2[b]] + [p for group in packs2[b] for p in group]
+            for d, h in zip(d_out, h_out2[b]):
+                h.copy_(d, non_blocking=True)
+        copied[b].record(copy_stream)
 
-    for _ in range(max(1, args.warmup)):
-        flush()
-        e2e_step()
+    for k in range(max(2, args.warmup)):
+        e2e_step(k)
     torch.cuda.synchronize()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
     for k in range(args.steps):
-        flush()
-        e2e_ev[k][0].record(stream)
-        e2e_step()
-        e2e_ev[k][1].record(stream)
+        e2e_step(k)
+    for e in copied:
+        stream.wait_event(e)
+    e_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    t_e2e = dist_max(np.mean([a.elapsed_time(b) for a, b in e2e_ev]) * 1e-3, ws)
+    t_e2e = dist_max(e_start.elapsed_time(e_end) * 1e-3 / args.steps, ws)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during timing")
 
@@ -500,7 +523,10 @@ def run_ours(args, ws, rank, local):
                      "cut segments are merged inside it)", "peak_source": peak_src},
         "e2e": {"value": round(replica_value(nb["step"], t_e2e, ws), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "note": "inputs copied in from pinned memory and output + packed KV copied "
+                        "out every step; copy-out of step k overlaps step k+1 (two buffer "
+                        "sets, copy stream)"},
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed": round(t_wall, 4),
         "clocks": clk.summary(),
