@@ -672,7 +672,7 @@ def sweep_workloads(args, dev, flush, peak):
         for cap in caps:
             out = torch.empty_like(s.q)
             wsp = workspace_for(s, cap)
-            for _ in range(3):
+            for _ in range(5):  # 5 warm-up launches, then the median of sweep_iters (50)
                 flush()
                 attention(s, out, cap, wsp)
             ts = []
@@ -860,7 +860,7 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="fewer requests (profiling only)")
     ap.add_argument("--sm-cap", type=int, default=0, help="SMs the attention may use (0: all)")
     ap.add_argument("--no-sweeps", dest="sweeps", action="store_false")
-    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--sweep-iters", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
