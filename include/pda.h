@@ -172,8 +172,11 @@ pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_ca
  * dequantised to FP8 before attention, raises memory bandwidth and throughput). Each
  * stored K code means decode(code) * k_scale and each V code decode(code) * v_scale
  * (per-tensor scales); the result is softmax(scale * q K^T) V over those values, exactly as
- * pda_paged_decode_attention computes it. Codes are widened exactly in registers and all
- * arithmetic is fp32.
+ * pda_paged_decode_attention computes it. Codes are widened exactly in registers. At D = 128
+ * the products run on the tensor cores: K, V (exact in fp16) and q (exact in fp16 after a
+ * power-of-two rescale) as fp16 operands, fp32 accumulation, probabilities entering P V as
+ * two fp16 parts (relative error about 2^-22); softmax in fp32. At D = 64 all arithmetic is
+ * fp32.
  *
  *  k_cache, v_cache [num_blocks, block_size, H_kv, D] bytes (E4M3 codes).
  *  q               [B, H, D] in q_dtype, which must be PDA_BF16.
@@ -201,9 +204,10 @@ pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* 
  *   code        = nibble d % 2 (0: low, 1: high) of k_data[r][h][d / 2],
  *   block scale = k_block_scales[r][h][d / 16]   (one per 16 consecutive elements),
  * and the same for V. E2M1 is the 4-bit float with 2 exponent bits (bias 1) and 1 mantissa
- * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Values are widened exactly to fp32 in
- * registers (the pages describe a dequantisation to FP8 before attention; fp32 holds every
- * product e2m1 * e4m3 exactly, so nothing is rounded before the softmax arithmetic).
+ * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Values are dequantised exactly in registers
+ * (the pages describe a dequantisation to FP8 before attention; fp16 and fp32 hold every
+ * product e2m1 * e4m3 exactly, so nothing is rounded before the attention arithmetic),
+ * which at D = 128 runs on the tensor cores as for pda_paged_decode_attention_fp8.
  *
  *  k_data, v_data   [num_blocks, block_size, H_kv, D / 2] bytes.
  *  k_block_scales, v_block_scales [num_blocks, block_size, H_kv, D / 16] E4M3 bytes,

@@ -31,7 +31,9 @@
 //    products of length D against 2 * D * sizeof(elem) bytes, and the bf16 path already
 //    streams at the HBM rate. Quantised caches (FP8, NVFP4) at D = 128 carry two to four
 //    times as many tokens per byte, so their dot products go to the tensor cores
-//    (warp_attn_tc.cuh); the pipeline, scheduling and merge below are shared.
+//    (warp_attn_tc.cuh), mostly on units of two adjacent kv-heads (one TMA box for both);
+//    the pipeline, scheduling and merge below are shared and see a pair as one unit with
+//    2 G query heads.
 #include <math.h>
 
 #include <atomic>
