@@ -192,21 +192,102 @@ int oracle_kv_unpack_blocks(const void* in, void* k_cache, void* v_cache,
 }
 
 /*
- * Element d of kv-head hk in cache row `row` (= block * block_size + offset), before the
- * per-tensor scale. NVFP4 (the 4-bit KV format with fine-grained E4M3 block scales, page
- * "From PagedAttention to Prefill-Decode disaggregation", sec. 6.2): the data tensor is
- * [rows, H_kv, D/2] bytes holding two E2M1 codes each, element d in the low nibble of byte
- * d/2 when d is even and in the high nibble when d is odd; the scale tensor is
- * [rows, H_kv, D/16] E4M3 bytes, one per 16 consecutive elements. The element's value is
+ * The same three copies for an NVFP4 block-scale cache, laid out per block and kv-head:
+ * [num_blocks, H_kv, block_size, row_bytes] (row_bytes = D/16 scale bytes). The new rows
+ * and the transfer buffer keep the token-major order of the data: new [B, H_kv, row_bytes],
+ * buffer [context_len, 2, H_kv, row_bytes]. Scale row of (token slot s, kv-head h): block
+ * s / block_size, offset s % block_size, at ((block * H_kv + h) * block_size + offset).
+ */
+static size_t orc_scale_row(int64_t block, int64_t offset, int h, int H_kv, int block_size) {
+  return ((size_t)block * (size_t)H_kv + (size_t)h) * (size_t)block_size + (size_t)offset;
+}
+
+int oracle_kv_append_block_scales(const void* k_new, const void* v_new, void* k_scales,
+                                  void* v_scales, const int32_t* slot_mapping, int B, int H_kv,
+                                  int row_bytes, int block_size, int num_blocks) {
+  if (B < 0 || H_kv <= 0 || row_bytes <= 0 || block_size <= 0 || num_blocks <= 0)
+    return ORC_ERR_ARG;
+  int status = ORC_OK;
+  for (int b = 0; b < B; ++b) {
+    const int32_t s = slot_mapping[b];
+    if (s < 0) continue;
+    if ((int64_t)s >= (int64_t)num_blocks * block_size) {
+      status = ORC_ERR_DATA;
+      continue;
+    }
+    for (int h = 0; h < H_kv; ++h) {
+      const size_t dst = orc_scale_row(s / block_size, s % block_size, h, H_kv, block_size) *
+                         (size_t)row_bytes;
+      const size_t src = ((size_t)b * (size_t)H_kv + (size_t)h) * (size_t)row_bytes;
+      memcpy((char*)k_scales + dst, (const char*)k_new + src, (size_t)row_bytes);
+      memcpy((char*)v_scales + dst, (const char*)v_new + src, (size_t)row_bytes);
+    }
+  }
+  return status;
+}
+
+int oracle_kv_pack_block_scales(void* out, const void* k_scales, const void* v_scales,
+                                const int32_t* block_table_row, int context_len, int H_kv,
+                                int row_bytes, int block_size, int num_blocks) {
+  if (context_len < 0 || H_kv <= 0 || row_bytes <= 0 || block_size <= 0 || num_blocks <= 0)
+    return ORC_ERR_ARG;
+  for (int t = 0; t < context_len; ++t) {
+    const int32_t block = block_table_row[t / block_size];
+    if (block < 0 || block >= num_blocks) return ORC_ERR_DATA;
+    for (int h = 0; h < H_kv; ++h) {
+      const size_t src =
+          orc_scale_row(block, t % block_size, h, H_kv, block_size) * (size_t)row_bytes;
+      char* dst = (char*)out + (((size_t)t * 2u) * (size_t)H_kv + (size_t)h) * (size_t)row_bytes;
+      memcpy(dst, (const char*)k_scales + src, (size_t)row_bytes);
+      memcpy(dst + (size_t)H_kv * (size_t)row_bytes, (const char*)v_scales + src,
+             (size_t)row_bytes);
+    }
+  }
+  return ORC_OK;
+}
+
+int oracle_kv_unpack_block_scales(const void* in, void* k_scales, void* v_scales,
+                                  const int32_t* block_table_row, int context_len, int H_kv,
+                                  int row_bytes, int block_size, int num_blocks) {
+  if (context_len < 0 || H_kv <= 0 || row_bytes <= 0 || block_size <= 0 || num_blocks <= 0)
+    return ORC_ERR_ARG;
+  int status = ORC_OK;
+  for (int t = 0; t < context_len; ++t) {
+    const int32_t block = block_table_row[t / block_size];
+    if (block < 0 || block >= num_blocks) {
+      status = ORC_ERR_DATA;
+      continue;
+    }
+    for (int h = 0; h < H_kv; ++h) {
+      const size_t dst =
+          orc_scale_row(block, t % block_size, h, H_kv, block_size) * (size_t)row_bytes;
+      const char* src =
+          (const char*)in + (((size_t)t * 2u) * (size_t)H_kv + (size_t)h) * (size_t)row_bytes;
+      memcpy((char*)k_scales + dst, src, (size_t)row_bytes);
+      memcpy((char*)v_scales + dst, src + (size_t)H_kv * (size_t)row_bytes, (size_t)row_bytes);
+    }
+  }
+  return status;
+}
+
+/*
+ * Element d of kv-head hk in row `offset` of physical block `block`, before the per-tensor
+ * scale. NVFP4 (the 4-bit KV format with fine-grained E4M3 block scales, page "From
+ * PagedAttention to Prefill-Decode disaggregation", sec. 6.2): the data tensor is
+ * [num_blocks, block_size, H_kv, D/2] bytes holding two E2M1 codes each, element d in the low
+ * nibble of byte d/2 when d is even and in the high nibble when d is odd; the scale tensor
+ * holds one E4M3 byte per 16 consecutive elements, laid out per block and kv-head,
+ * [num_blocks, H_kv, block_size, D/16]. The element's value is
  * e2m1(code) * e4m3(scale of its 16-element block).
  */
-static double orc_kv(const void* cache, const void* block_scales, size_t row, int hk, int d,
-                     int H_kv, int D, int dtype) {
-  const size_t r = row * (size_t)H_kv + (size_t)hk;
+static double orc_kv(const void* cache, const void* block_scales, size_t block, size_t offset,
+                     int block_size, int hk, int d, int H_kv, int D, int dtype) {
+  const size_t r = (block * (size_t)block_size + offset) * (size_t)H_kv + (size_t)hk;
   if (dtype == ORC_NVFP4) {
     const uint8_t byte = ((const uint8_t*)cache)[r * (size_t)(D / 2) + (size_t)(d / 2)];
     const unsigned code = (d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15);
-    const uint8_t sc = ((const uint8_t*)block_scales)[r * (size_t)(D / 16) + (size_t)(d / 16)];
+    const size_t srow = (block * (size_t)H_kv + (size_t)hk) * (size_t)block_size + offset;
+    const uint8_t sc = ((const uint8_t*)block_scales)[srow * (size_t)(D / 16) + (size_t)(d / 16)];
     return orc_e2m1(code) * orc_e4m3(sc);
   }
   return orc_load(cache, r * (size_t)D + (size_t)d, dtype);
@@ -224,10 +305,12 @@ static int orc_gather(double* Kc, double* Vc, const void* k_cache, const void* v
   for (int t = 0; t < L; ++t) {
     const int32_t block = table_row[t / block_size];
     if (block < 0 || block >= num_blocks) return -1;
-    const size_t row = (size_t)block * (size_t)block_size + (size_t)(t % block_size);
+    const size_t off = (size_t)(t % block_size);
     for (int d = 0; d < D; ++d) {
-      Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype) * k_scale;
-      Vc[(size_t)t * D + d] = orc_kv(v_cache, v_bs, row, hk, d, H_kv, D, kv_dtype) * v_scale;
+      Kc[(size_t)t * D + d] =
+          orc_kv(k_cache, k_bs, (size_t)block, off, block_size, hk, d, H_kv, D, kv_dtype) * k_scale;
+      Vc[(size_t)t * D + d] =
+          orc_kv(v_cache, v_bs, (size_t)block, off, block_size, hk, d, H_kv, D, kv_dtype) * v_scale;
     }
   }
   return 0;
@@ -333,7 +416,7 @@ int oracle_paged_decode_attention(double* out, const void* q, const void* k_cach
 
 /*
  * The same attention over an NVFP4 cache: k_data/v_data are [num_blocks, block_size, H_kv,
- * D/2] bytes, k_block_scales/v_block_scales [num_blocks, block_size, H_kv, D/16] E4M3 bytes;
+ * D/2] bytes, k_block_scales/v_block_scales [num_blocks, H_kv, block_size, D/16] E4M3 bytes;
  * a K element means e2m1(code) * e4m3(block scale) * k_scale (see orc_kv).
  */
 int oracle_paged_decode_attention_nvfp4(double* out, const void* q, const void* k_data,

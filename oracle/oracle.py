@@ -70,6 +70,13 @@ def load(path: str | None = None):
         lib.oracle_attention_partial.restype = I
         lib.oracle_lse_combine.argtypes = [I, P, P, P, I, P]
         lib.oracle_lse_combine.restype = I
+        # NVFP4 block-scale caches [num_blocks, H_kv, block_size, row_bytes]
+        lib.oracle_kv_append_block_scales.argtypes = [P, P, P, P, P, I, I, I, I, I]
+        lib.oracle_kv_append_block_scales.restype = I
+        lib.oracle_kv_pack_block_scales.argtypes = [P, P, P, P, I, I, I, I, I]
+        lib.oracle_kv_pack_block_scales.restype = I
+        lib.oracle_kv_unpack_block_scales.argtypes = [P, P, P, P, I, I, I, I, I]
+        lib.oracle_kv_unpack_block_scales.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -132,13 +139,13 @@ def paged_decode_attention_nvfp4(q, k_data, v_data, k_block_scales, v_block_scal
                                  block_tables, context_lens, scale: float, k_scale: float = 1.0,
                                  v_scale: float = 1.0, num_threads: int = 0, lib=None):
     """fp64 attention over an NVFP4 cache: data [NB, bs, H_kv, D/2] uint8 (two E2M1 codes
-    per byte, even element in the low nibble), block scales [NB, bs, H_kv, D/16] uint8
-    (E4M3). Returns (out[B,H,D] float64, status)."""
+    per byte, even element in the low nibble), block scales [NB, H_kv, bs, D/16] uint8
+    (E4M3, per block and kv-head). Returns (out[B,H,D] float64, status)."""
     lib = lib or load()
     B, H, D = q.shape
     NB, bs, H_kv, half = k_data.shape
     assert half * 2 == D and k_data.dtype == np.uint8 and v_data.shape == k_data.shape
-    assert k_block_scales.shape == (NB, bs, H_kv, D // 16) == v_block_scales.shape
+    assert k_block_scales.shape == (NB, H_kv, bs, D // 16) == v_block_scales.shape
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
     out = np.zeros((B, H, D), dtype=np.float64)
@@ -206,3 +213,40 @@ def lse_combine(m, l_, o, lib=None):
     if st != ORC_OK:
         raise RuntimeError(f"oracle_lse_combine failed with status {st}")
     return out
+
+
+def kv_append_block_scales(k_new, v_new, k_scales, v_scales, slot_mapping, lib=None) -> int:
+    """In-place append of one token's scale rows per request into NVFP4 block-scale caches
+    [NB, H_kv, bs, R] (new rows [B, H_kv, R]); returns the status."""
+    lib = lib or load()
+    NB, H_kv, bs, R = k_scales.shape
+    B = slot_mapping.shape[0]
+    assert k_new.shape == (B, H_kv, R) == v_new.shape and k_scales.dtype == np.uint8
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    return lib.oracle_kv_append_block_scales(_ptr(k_new), _ptr(v_new), _ptr(k_scales),
+                                             _ptr(v_scales), _ptr(slot_mapping), B, H_kv, R,
+                                             bs, NB)
+
+
+def kv_pack_block_scales(k_scales, v_scales, block_table_row, context_len: int, lib=None):
+    """One request's scale rows from block-scale caches [NB, H_kv, bs, R] into a dense
+    token-major [L, 2, H_kv, R] buffer; returns (out, status)."""
+    lib = lib or load()
+    NB, H_kv, bs, R = k_scales.shape
+    out = np.zeros((context_len, 2, H_kv, R), dtype=np.uint8)
+    row = np.ascontiguousarray(block_table_row, dtype=np.int32)
+    st = lib.oracle_kv_pack_block_scales(_ptr(out), _ptr(k_scales), _ptr(v_scales), _ptr(row),
+                                         int(context_len), H_kv, R, bs, NB)
+    return out, st
+
+
+def kv_unpack_block_scales(packed, k_scales, v_scales, block_table_row, context_len: int,
+                           lib=None) -> int:
+    """The inverse of kv_pack_block_scales, in place; returns the status."""
+    lib = lib or load()
+    NB, H_kv, bs, R = k_scales.shape
+    assert packed.shape[1:] == (2, H_kv, R)
+    row = np.ascontiguousarray(block_table_row, dtype=np.int32)
+    return lib.oracle_kv_unpack_block_scales(_ptr(np.ascontiguousarray(packed)), _ptr(k_scales),
+                                             _ptr(v_scales), _ptr(row), int(context_len),
+                                             H_kv, R, bs, NB)

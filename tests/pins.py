@@ -399,9 +399,9 @@ def pin_nvfp4_attention_brute_force(lib):
         NB = sum(nblk) + 2
         kd = rng.integers(0, 256, (NB, bs, H_kv, D // 2)).astype(np.uint8)
         vd = rng.integers(0, 256, (NB, bs, H_kv, D // 2)).astype(np.uint8)
-        # block scales: E4M3 codes of 0.25 .. 0.47 (exponent field 5)
-        ks = rng.integers(0x28, 0x30, (NB, bs, H_kv, D // 16)).astype(np.uint8)
-        vs = rng.integers(0x28, 0x30, (NB, bs, H_kv, D // 16)).astype(np.uint8)
+        # block scales: E4M3 codes of 0.25 .. 0.47 (exponent field 5), per block and kv-head
+        ks = rng.integers(0x28, 0x30, (NB, H_kv, bs, D // 16)).astype(np.uint8)
+        vs = rng.integers(0x28, 0x30, (NB, H_kv, bs, D // 16)).astype(np.uint8)
         perm = rng.permutation(NB).astype(np.int32)
         bt = np.full((B, max(nblk)), -1, np.int32)
         off = 0
@@ -424,10 +424,50 @@ def pin_nvfp4_attention_brute_force(lib):
 
         for b, L in enumerate(lengths):
             rows = [(bt[b, t // bs], t % bs) for t in range(L)]
-            K = np.stack([dequant(kd[r], ks[r], k_scale) for r in rows])
-            V = np.stack([dequant(vd[r], vs[r], v_scale) for r in rows])
+            K = np.stack([dequant(kd[r], ks[r[0], :, r[1]], k_scale) for r in rows])
+            V = np.stack([dequant(vd[r], vs[r[0], :, r[1]], v_scale) for r in rows])
             ref = brute.dense_decode_attention(stored_to_f64(q[b]), K, V, scale)
             assert np.abs(out[b] - ref).max() <= 1e-12, (lengths, b)
+
+
+def pin_block_scale_copies(lib):
+    """NVFP4 block-scale caches [NB, H_kv, bs, R]: append puts request b's row of kv-head h at
+    [slot // bs, h, slot % bs]; pack reads [block, h, row] into the token-major buffer
+    [t, 0|1, h]; unpack writes it back. Checked against numpy indexing of that layout."""
+    rng = np.random.default_rng(31)
+    NB, H_kv, bs, R = 7, 3, 4, 8
+    ks = rng.integers(0, 256, (NB, H_kv, bs, R)).astype(np.uint8)
+    vs = rng.integers(0, 256, (NB, H_kv, bs, R)).astype(np.uint8)
+    k0, v0 = ks.copy(), vs.copy()
+    slots = np.array([5, -1, 26, 13], np.int32)  # (1, 1), padding, (6, 2), (3, 1)
+    kn = rng.integers(0, 256, (4, H_kv, R)).astype(np.uint8)
+    vn = rng.integers(0, 256, (4, H_kv, R)).astype(np.uint8)
+    assert orc.kv_append_block_scales(kn, vn, ks, vs, slots, lib=lib) == orc.ORC_OK
+    want_k, want_v = k0.copy(), v0.copy()
+    for b, sl in enumerate(slots):
+        if sl >= 0:
+            want_k[sl // bs, :, sl % bs] = kn[b]
+            want_v[sl // bs, :, sl % bs] = vn[b]
+    assert np.array_equal(ks, want_k) and np.array_equal(vs, want_v)
+    table = np.array([6, 1, 3], np.int32)
+    L = 10
+    packed, st = orc.kv_pack_block_scales(ks, vs, table, L, lib=lib)
+    assert st == orc.ORC_OK and packed.shape == (L, 2, H_kv, R)
+    for t in range(L):
+        blk, off = table[t // bs], t % bs
+        assert np.array_equal(packed[t, 0], ks[blk, :, off])
+        assert np.array_equal(packed[t, 1], vs[blk, :, off])
+    k2, v2 = np.zeros_like(ks), np.zeros_like(vs)
+    assert orc.kv_unpack_block_scales(packed, k2, v2, table, L, lib=lib) == orc.ORC_OK
+    for t in range(L):
+        blk, off = table[t // bs], t % bs
+        assert np.array_equal(k2[blk, :, off], ks[blk, :, off])
+    touched = np.zeros((NB, bs), bool)
+    for t in range(L):
+        touched[table[t // bs], t % bs] = True
+    assert not k2.transpose(0, 2, 1, 3)[~touched].any()  # nothing else written
+    bad = np.array([6, NB + 2, 3], np.int32)
+    assert orc.kv_pack_block_scales(ks, vs, bad, L, lib=lib)[1] == orc.ORC_ERR_DATA
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

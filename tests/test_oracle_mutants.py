@@ -62,12 +62,24 @@ MUTANTS = [
      [("(d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15)",
        "(d & 1) ? (unsigned)(byte & 15) : (unsigned)(byte >> 4)", None)]),
     ("nvfp4_wrong_block_index",
-     [("r * (size_t)(D / 16) + (size_t)(d / 16)", "r * (size_t)(D / 16) + (size_t)(d / 32)", None)]),
+     [("srow * (size_t)(D / 16) + (size_t)(d / 16)", "srow * (size_t)(D / 16) + (size_t)(d / 32)",
+       None)]),
+    ("nvfp4_scales_read_token_major",
+     [("const size_t srow = (block * (size_t)H_kv + (size_t)hk) * (size_t)block_size + offset;",
+       "const size_t srow = (block * (size_t)block_size + offset) * (size_t)H_kv + (size_t)hk;",
+       None)]),
+    ("block_scale_rows_token_major",
+     [("return ((size_t)block * (size_t)H_kv + (size_t)h) * (size_t)block_size + (size_t)offset;",
+       "return ((size_t)block * (size_t)block_size + (size_t)offset) * (size_t)H_kv + (size_t)h;",
+       None)]),
+    ("block_scale_pack_swaps_k_and_v",
+     [("memcpy(dst, (const char*)k_scales + src, (size_t)row_bytes);",
+       "memcpy(dst, (const char*)v_scales + src, (size_t)row_bytes);", None)]),
     ("nvfp4_block_scale_dropped",
      [("return orc_e2m1(code) * orc_e4m3(sc);", "(void)sc; return orc_e2m1(code);", None)]),
     ("kv_scale_dropped",
-     [("Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype) * k_scale;",
-       "Kc[(size_t)t * D + d] = orc_kv(k_cache, k_bs, row, hk, d, H_kv, D, kv_dtype);", None)]),
+     [("off, block_size, hk, d, H_kv, D, kv_dtype) * k_scale;",
+       "off, block_size, hk, d, H_kv, D, kv_dtype);", None)]),
 ]
 
 
