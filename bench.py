@@ -242,11 +242,16 @@ def barrier(ws):
 
 
 def kv_arrays(s):
-    """(cache K, cache V, new K, new V) byte arrays of a step: the codes, and for NVFP4 the
-    block scales too (appended, packed and unpacked as arrays of their own)."""
-    arrays = [(s.k_cache, s.v_cache, s.k_new, s.v_new)]
+    """Per stored array pair of a step: (cache K, cache V, new K, new V, append, batched pack,
+    batched unpack) -- the K/V rows, and for NVFP4 also the block scales, which have their
+    own calls (per-block head-major layout). The three calls share one argument order."""
+    import paged_decode_attention_02_gb300 as pda
+    arrays = [(s.k_cache, s.v_cache, s.k_new, s.v_new, pda.kv_append, pda.kv_pack_blocks_batched,
+               pda.kv_unpack_blocks_batched)]
     if s.w.kv == "nvfp4":
-        arrays.append((s.k_bscales, s.v_bscales, s.k_new_bscales, s.v_new_bscales))
+        arrays.append((s.k_bscales, s.v_bscales, s.k_new_bscales, s.v_new_bscales,
+                       pda.kv_append_block_scales, pda.kv_pack_block_scales_batched,
+                       pda.kv_unpack_block_scales_batched))
     return arrays
 
 
@@ -273,13 +278,13 @@ def oracle_pass(s, threads: int):
     kc, vc = _np(s.k_cache).copy(), _np(s.v_cache).copy()
     q, kn, vn = _np(s.q), _np(s.k_new), _np(s.v_new)
     nvfp4 = s.w.kv == "nvfp4"
-    if nvfp4:  # codes and block scales are appended and packed as two byte arrays
+    if nvfp4:  # codes and block scales are appended and packed apart
         ksc, vsc = _np(s.k_bscales).copy(), _np(s.v_bscales).copy()
         ksn, vsn = _np(s.k_new_bscales), _np(s.v_new_bscales)
     t0 = time.perf_counter()
     orc.kv_append(kn, vn, kc, vc, s.slot_mapping_np)
     if nvfp4:
-        orc.kv_append(ksn, vsn, ksc, vsc, s.slot_mapping_np)
+        orc.kv_append_block_scales(ksn, vsn, ksc, vsc, s.slot_mapping_np)
         orc.paged_decode_attention_nvfp4(q, kc, vc, ksc, vsc, s.block_tables_np,
                                          s.context_lens_np, s.scale, s.k_scale, s.v_scale,
                                          num_threads=threads)
@@ -289,7 +294,7 @@ def oracle_pass(s, threads: int):
     for r in s.pack_requests:
         orc.kv_pack_blocks(kc, vc, s.block_tables_np[r], int(s.context_lens_np[r]))
         if nvfp4:
-            orc.kv_pack_blocks(ksc, vsc, s.block_tables_np[r], int(s.context_lens_np[r]))
+            orc.kv_pack_block_scales(ksc, vsc, s.block_tables_np[r], int(s.context_lens_np[r]))
     return time.perf_counter() - t0
 
 
@@ -351,30 +356,28 @@ def run_ours(args, ws, rank, local):
     cap = args.sm_cap
     wsp = workspace_for(s, cap)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    # (cache K, cache V, new K, new V): the codes, and for NVFP4 also the block scales, each
-    # appended and packed as its own byte array
+    # the codes, and for NVFP4 also the block scales, each appended and packed by its calls
     arrays = kv_arrays(s)
     pack_rows = [s.block_tables[r] for r in pack_reqs]
     pack_lens = [int(s.context_lens_np[r]) for r in pack_reqs]
-    packs_of = [[torch.empty((L, 2) + tuple(kc.shape[2:]), dtype=kc.dtype, device=dev)
-                 for L in pack_lens] for kc, _, _, _ in arrays]
+    packs_of = [[torch.empty((L, 2) + tuple(kn.shape[1:]), dtype=kc.dtype, device=dev)
+                 for L in pack_lens] for kc, _, kn, _, _, _, _ in arrays]
     packs = [p for group in packs_of for p in group]
     launches_per_step = len(arrays) + 1 + (len(arrays) if pack_reqs else 0)
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        for kc, vc, kn, vn in arrays:
-            pda.kv_append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
+        for kc, vc, kn, vn, append, _, _ in arrays:
+            append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
         if ev:
             ev[1].record(stream)
         attention(s, out, cap, wsp, error_word=err)
         if ev:
             ev[2].record(stream)
         if pack_reqs:
-            for (kc, vc, _, _), group in zip(arrays, packs_of):
-                pda.kv_pack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
-                                           error_word=err)
+            for (kc, vc, _, _, _, pack, _), group in zip(arrays, packs_of):
+                pack(group, kc, vc, pack_rows, pack_lens, error_word=err)
         if ev:
             ev[3].record(stream)
 
@@ -411,7 +414,7 @@ def run_ours(args, ws, rank, local):
     # sets of output buffers, the copies on their own stream; step k waits only for the
     # copy-out that last used its buffer set. Timed over the whole loop (inputs larger than
     # L2, so no flush inside it).
-    d_in = [s.q] + [t for _, _, kn, vn in arrays for t in (kn, vn)] + [
+    d_in = [s.q] + [t for _, _, kn, vn, _, _, _ in arrays for t in (kn, vn)] + [
         s.slot_mapping, s.block_tables, s.context_lens]
     h_in = [x.detach().cpu().pin_memory() for x in d_in]
     outs2 = [out, torch.empty_like(out)]
@@ -431,13 +434,12 @@ def run_ours(args, ws, rank, local):
         stream.wait_event(copied[b])  # buffer set b is free again
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        for kc, vc, kn, vn in arrays:
-            pda.kv_append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
+        for kc, vc, kn, vn, append, _, _ in arrays:
+            append(kn, vn, kc, vc, s.slot_mapping, error_word=err)
         attention(s, outs2[b], cap, wsp, error_word=err)
         if pack_reqs:
-            for (kc, vc, _, _), group in zip(arrays, packs2[b]):
-                pda.kv_pack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
-                                           error_word=err)
+            for (kc, vc, _, _, _, pack, _), group in zip(arrays, packs2[b]):
+                pack(group, kc, vc, pack_rows, pack_lens, error_word=err)
         computed[b].record(stream)
         copy_stream.wait_event(computed[b])
         with torch.cuda.stream(copy_stream):
@@ -473,9 +475,8 @@ def run_ours(args, ws, rank, local):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             flush()
             a.record(stream)
-            for (kc, vc, _, _), group in zip(arrays, packs_of):
-                pda.kv_unpack_blocks_batched(group, kc, vc, pack_rows, pack_lens,
-                                             error_word=err)
+            for (kc, vc, _, _, _, _, unpack), group in zip(arrays, packs_of):
+                unpack(group, kc, vc, pack_rows, pack_lens, error_word=err)
             b.record(stream)
             uev.append((a, b))
         torch.cuda.synchronize()

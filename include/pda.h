@@ -55,8 +55,8 @@ typedef enum {
 /* Element types. PDA_FP8_E4M3 (the OCP 8-bit format without infinities) is a KV-cache type
  * only: append, pack and unpack copy its bytes, and pda_paged_decode_attention_fp8 reads it
  * with per-tensor scales. PDA_NVFP4 names the 4-bit cache read by
- * pda_paged_decode_attention_nvfp4 (and sizes its workspace); its data and scale tensors are
- * plain byte arrays that append, pack and unpack copy as 1-byte elements (see that call). */
+ * pda_paged_decode_attention_nvfp4 (and sizes its workspace); its data tensors are moved as
+ * 1-byte rows by append, pack and unpack, its block scales by the *_block_scales calls. */
 typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2, PDA_NVFP4 = 3 } pda_dtype;
 
 /* Bits OR-ed into *error_word by the kernels. */
@@ -202,7 +202,8 @@ pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* 
  * block scales and E4M3 scale factors). Element d of the K row of (token row r, kv-head h)
  * means  e2m1(code) * e4m3(block scale) * k_scale,  with
  *   code        = nibble d % 2 (0: low, 1: high) of k_data[r][h][d / 2],
- *   block scale = k_block_scales[r][h][d / 16]   (one per 16 consecutive elements),
+ *   block scale = k_block_scales[r / block_size][h][r % block_size][d / 16]
+ *                 (one per 16 consecutive elements),
  * and the same for V. E2M1 is the 4-bit float with 2 exponent bits (bias 1) and 1 mantissa
  * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Values are dequantised exactly in registers
  * (the pages describe a dequantisation to FP8 before attention; fp16 and fp32 hold every
@@ -210,16 +211,20 @@ pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* 
  * which at D = 128 runs on the tensor cores as for pda_paged_decode_attention_fp8.
  *
  *  k_data, v_data   [num_blocks, block_size, H_kv, D / 2] bytes.
- *  k_block_scales, v_block_scales [num_blocks, block_size, H_kv, D / 16] E4M3 bytes,
- *                   16-byte aligned.
+ *  k_block_scales, v_block_scales [num_blocks, H_kv, block_size, D / 16] E4M3 bytes,
+ *                   16-byte aligned: per block and head-major, so the scales of one
+ *                   (block, kv-head) tile are one contiguous run of block_size * D / 16
+ *                   bytes (the pages give no layout; this is the one the kernel reads in
+ *                   one bulk copy per tile).
  *  q                [B, H, D] in q_dtype, which must be PDA_BF16.
  *  k_scale, v_scale finite per-tensor scales.
  *  Every other argument, the workspace (pda_attention_workspace_size with PDA_NVFP4), the
  *  supported sizes and the errors are those of pda_paged_decode_attention.
- *  Append, pack and unpack: both tensors are token-major byte caches, so pda_kv_append,
- *  pda_kv_pack_blocks[_batched] and pda_kv_unpack_blocks[_batched] move them with kv_dtype
- *  PDA_FP8_E4M3 (any 1-byte type) and D / 2 (data) or D / 16 (scales) as the row length,
- *  one call per tensor pair; each needs H_kv * row length to be a multiple of 16 bytes.
+ *  Append, pack and unpack: the data tensors are token-major byte caches, moved by
+ *  pda_kv_append, pda_kv_pack_blocks[_batched] and pda_kv_unpack_blocks[_batched] with
+ *  kv_dtype PDA_FP8_E4M3 (any 1-byte type) and D / 2 as the row length (H_kv * D / 2 a
+ *  multiple of 16 bytes); the block scales by pda_kv_append_block_scales,
+ *  pda_kv_pack_block_scales_batched and pda_kv_unpack_block_scales_batched.
  */
 pda_status pda_paged_decode_attention_nvfp4(void* out, const void* q, const void* k_data,
                                             const void* v_data, const void* k_block_scales,
@@ -378,6 +383,62 @@ pda_status pda_kv_unpack_layers(const void* const* ins, void* const* k_caches,
                                 const int32_t* block_table_row, int context_len, int H_kv,
                                 int D, int block_size, int num_blocks, pda_dtype kv_dtype,
                                 int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_append_block_scales -- pda_kv_append for the E4M3 block scales of an NVFP4 cache.
+ *
+ * Each decode step's new token brings one scale per 16 elements of its K and V rows (page
+ * "From PagedAttention to Prefill-Decode disaggregation", sec. 6.2, NVFP4 KV with block
+ * scales); the token of request b goes to slot s = slot_mapping[b], i.e. row s % block_size of
+ * block s / block_size (page "Disaggregated LLM Serving: from PD disaggregation to attention
+ * offload", sec. 1, the per-step KV write). For b < B and h < H_kv:
+ *      k_scales[s / block_size][h][s % block_size][:] = k_new[b][h][:]   (D / 16 bytes)
+ * and the same for V.
+ *
+ *  k_new, v_new     [B, H_kv, D / 16] E4M3 bytes, 4-byte aligned; read only.
+ *  k_scales, v_scales [num_blocks, H_kv, block_size, D / 16] (the layout of
+ *                   pda_paged_decode_attention_nvfp4), 4-byte aligned; updated in place.
+ *  slot_mapping     [B] int32, device; negative = padding (skipped).
+ *  D a multiple of 64 (rows move as 4-byte words), else PDA_ERR_UNSUPPORTED. A slot at or
+ *  beyond num_blocks * block_size sets PDA_DEVERR_SLOT and is skipped. B = 0 is a no-op.
+ */
+pda_status pda_kv_append_block_scales(const void* k_new, const void* v_new, void* k_scales,
+                                      void* v_scales, const int32_t* slot_mapping, int B,
+                                      int H_kv, int D, int block_size, int num_blocks,
+                                      int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_pack_block_scales_batched -- pda_kv_pack_blocks_batched for the block scales of an
+ * NVFP4 cache: for request i and t < context_lens[i], with block = block_table_rows[i][t /
+ * block_size] and offset = t % block_size,
+ *      outs[i][t, 0, h, :] = k_scales[block][h][offset][:],
+ *      outs[i][t, 1, h, :] = v_scales[block][h][offset][:].
+ *
+ *  outs[i]          [context_lens[i], 2, H_kv, D / 16] bytes, dense, 4-byte aligned.
+ *  outs, block_table_rows, context_lens: HOST arrays of n entries (device pointers and host
+ *  counts), copied into the launch. n <= PDA_PACK_MAX_BATCH. A block id out of range sets
+ *  PDA_DEVERR_BLOCK_ID and fills that token's scales with 0xFF bytes (an E4M3 NaN).
+ *  D a multiple of 64. Bitwise copy.
+ */
+pda_status pda_kv_pack_block_scales_batched(void* const* outs,
+                                            const int32_t* const* block_table_rows,
+                                            const int32_t* context_lens, int n,
+                                            const void* k_scales, const void* v_scales,
+                                            int H_kv, int D, int block_size, int num_blocks,
+                                            int32_t* error_word, cudaStream_t stream);
+
+/*
+ * pda_kv_unpack_block_scales_batched -- the inverse of pda_kv_pack_block_scales_batched:
+ * k_scales[block][h][offset][:] = ins[i][t, 0, h, :] and v_scales[...] = ins[i][t, 1, h, :].
+ * A block id out of range sets PDA_DEVERR_BLOCK_ID and that token is not written; other
+ * rows are not touched. Arrays, limits and alignment as for the pack.
+ */
+pda_status pda_kv_unpack_block_scales_batched(const void* const* ins,
+                                              const int32_t* const* block_table_rows,
+                                              const int32_t* context_lens, int n,
+                                              void* k_scales, void* v_scales, int H_kv, int D,
+                                              int block_size, int num_blocks,
+                                              int32_t* error_word, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,8 @@ EXPORTED = [
     "pda_kv_pack_blocks_batched", "pda_paged_decode_attention_noalloc",
     "pda_kv_unpack_blocks", "pda_kv_unpack_blocks_batched", "pda_paged_decode_attention_fp8",
     "pda_paged_decode_attention_nvfp4", "pda_kv_pack_layers", "pda_kv_unpack_layers",
+    "pda_kv_append_block_scales", "pda_kv_pack_block_scales_batched",
+    "pda_kv_unpack_block_scales_batched",
 ]
 
 _lock = threading.Lock()
@@ -91,6 +93,13 @@ def load():
         lib.pda_kv_pack_layers.restype = I
         lib.pda_kv_unpack_layers.argtypes = [P, P, P, I, P, I, I, I, I, I, I, P, P]
         lib.pda_kv_unpack_layers.restype = I
+        # NVFP4 block scales: news/caches, slots or (bufs, rows, lens, n), H_kv, D, bs, NB, ...
+        lib.pda_kv_append_block_scales.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
+        lib.pda_kv_append_block_scales.restype = I
+        lib.pda_kv_pack_block_scales_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P]
+        lib.pda_kv_pack_block_scales_batched.restype = I
+        lib.pda_kv_unpack_block_scales_batched.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P]
+        lib.pda_kv_unpack_block_scales_batched.restype = I
         _lib = lib
         return lib
 
@@ -236,11 +245,12 @@ def paged_decode_attention_nvfp4(out, q, k_data, v_data, k_block_scales, v_block
                                  k_scale: float, v_scale: float, sm_cap: int = 0, workspace=None,
                                  error_word=None, stream=None):
     """Attention over an NVFP4 cache: data [NB, bs, H_kv, D/2] uint8 (two E2M1 codes per
-    byte, even element low), block scales [NB, bs, H_kv, D/16] uint8 (E4M3)."""
+    byte, even element low), block scales [NB, H_kv, bs, D/16] uint8 (E4M3, per block and
+    head-major)."""
     B, H, D = q.shape
     NB, bs, H_kv, half = k_data.shape
     assert 2 * half == D and v_data.shape == k_data.shape and out.shape == q.shape
-    assert tuple(k_block_scales.shape) == (NB, bs, H_kv, D // 16)
+    assert tuple(k_block_scales.shape) == (NB, H_kv, bs, D // 16)
     assert v_block_scales.shape == k_block_scales.shape
     assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
     max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
@@ -338,6 +348,54 @@ def kv_unpack_blocks_batched(packed, k_cache, v_cache, block_table_rows, context
                                                _ptr(v_cache), H_kv, D, bs, NB, _dtype(k_cache),
                                                _ptr(error_word), _stream(stream)),
            "pda_kv_unpack_blocks_batched")
+
+
+def kv_append_block_scales(k_new, v_new, k_scales, v_scales, slot_mapping, error_word=None,
+                           stream=None):
+    """Scatter each request's new NVFP4 block scales (``[B, H_kv, D/16]`` uint8) into the
+    ``[NB, H_kv, bs, D/16]`` scale caches at its slot."""
+    NB, H_kv, bs, S = k_scales.shape
+    B = slot_mapping.shape[0]
+    assert k_new.shape == (B, H_kv, S) and v_new.shape == (B, H_kv, S)
+    assert v_scales.shape == k_scales.shape and slot_mapping.dtype == torch.int32
+    _check(load().pda_kv_append_block_scales(_ptr(k_new), _ptr(v_new), _ptr(k_scales),
+                                             _ptr(v_scales), _ptr(slot_mapping), B, H_kv,
+                                             16 * S, bs, NB, _ptr(error_word),
+                                             _stream(stream)), "pda_kv_append_block_scales")
+
+
+def _scale_arrays(bufs, block_table_rows, context_lens, shape_tail):
+    n = len(bufs)
+    assert len(block_table_rows) == n and len(context_lens) == n
+    for b, L in zip(bufs, context_lens):
+        assert b.shape[0] >= int(L) and tuple(b.shape[1:]) == shape_tail
+    buf_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(x).value for x in bufs])
+    row_arr = (ctypes.c_void_p * max(n, 1))(*[_ptr(r).value for r in block_table_rows])
+    len_arr = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in context_lens])
+    return n, buf_arr, row_arr, len_arr
+
+
+def kv_pack_block_scales_batched(outs, k_scales, v_scales, block_table_rows, context_lens,
+                                 error_word=None, stream=None):
+    """Gather requests' NVFP4 block scales into ``outs[i][len_i, 2, H_kv, D/16]``."""
+    NB, H_kv, bs, S = k_scales.shape
+    n, o, r, l = _scale_arrays(outs, block_table_rows, context_lens, (2, H_kv, S))
+    _check(load().pda_kv_pack_block_scales_batched(o, r, l, n, _ptr(k_scales), _ptr(v_scales),
+                                                   H_kv, 16 * S, bs, NB, _ptr(error_word),
+                                                   _stream(stream)),
+           "pda_kv_pack_block_scales_batched")
+    return outs
+
+
+def kv_unpack_block_scales_batched(packed, k_scales, v_scales, block_table_rows,
+                                   context_lens, error_word=None, stream=None):
+    """Scatter requests' ``[len_i, 2, H_kv, D/16]`` scale buffers into the scale caches."""
+    NB, H_kv, bs, S = k_scales.shape
+    n, i, r, l = _scale_arrays(packed, block_table_rows, context_lens, (2, H_kv, S))
+    _check(load().pda_kv_unpack_block_scales_batched(i, r, l, n, _ptr(k_scales),
+                                                     _ptr(v_scales), H_kv, 16 * S, bs, NB,
+                                                     _ptr(error_word), _stream(stream)),
+           "pda_kv_unpack_block_scales_batched")
 
 
 def _layer_arrays(bufs, k_caches, v_caches):

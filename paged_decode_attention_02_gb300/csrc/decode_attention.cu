@@ -109,7 +109,7 @@ struct AttnParams {
   unsigned long long call;        // this call's number (48 bits)
   int32_t* error_word;
   float v_scale;                  // value of a stored V element = code * v_scale (1 if plain)
-  const uint8_t* k_bscales;       // NVFP4: [rows, H_kv, D/16] E4M3 block scales (else null)
+  const uint8_t* k_bscales;       // NVFP4: [blocks, H_kv, 16, D/16] E4M3 block scales
   const uint8_t* v_bscales;
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
   int out_bf16;
@@ -573,7 +573,6 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   constexpr int kHeads = MODE == kModeTcPair ? 2 : 1;
   constexpr uint32_t kTile = kHeads * Geo::TILE_BYTES;
   constexpr uint32_t kScales = kHeads * Geo::SCALE_BYTES;
-  constexpr int kRowScales = kHeads * Geo::ROW_SCALES;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // The host reserves stage_align(TC) - 128 spare bytes; the layout starts at the first
   // aligned address (swizzled TMA tiles need the swizzle period's alignment).
@@ -634,9 +633,8 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   }
   // barrier init (one lane per warp, its own stages)
   if (lane == 0) {
-    // one arrive carries the TMA byte count; NVFP4 adds one per lane for the scale copies
-    for (int s = 0; s < p.stages; ++s)
-      mbar_init(&s_bar[warp * p.stages + s], Geo::SCALED ? 33 : 1);
+    // one arrive carries the byte count of the stage's copies
+    for (int s = 0; s < p.stages; ++s) mbar_init(&s_bar[warp * p.stages + s], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -673,7 +671,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   auto v_buf = [&](int s) {
     return reinterpret_cast<KV*>(my_stage + s * p.stage_bytes + kTile);
   };
-  auto ks_buf = [&](int s) {  // NVFP4 block scales of the K tile, [16][D/16]
+  auto ks_buf = [&](int s) {  // NVFP4 block scales of the K tile, [kHeads][16][D/16]
     return reinterpret_cast<uint8_t*>(my_stage + s * p.stage_bytes + 2 * kTile);
   };
   auto vs_buf = [&](int s) {
@@ -738,30 +736,21 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   enter(t_begin, 0);
   auto issue = [&](int x, int s) {
     if (x >= g_base + 32) enter(g_base + 32, g_buf ^ 1);
-    if constexpr (Geo::SCALED) {
-      // lanes 0-15 copy the 16 K scale rows of the tile, lanes 16-31 the V rows; each copy
-      // arrives on the stage barrier when it lands
-      const int src_lane = x - g_base;
-      int pid = __shfl_sync(kFullMask, cur_pid, src_lane);
-      const int h = __shfl_sync(kFullMask, cur_h, src_lane);
-      if (pid < 0 || pid >= p.num_blocks) pid = 0;  // flagged below; read a valid block
-      const int r = lane & 15;
-      const bool is_v = lane >= 16;
-      const uint8_t* src = (is_v ? p.v_bscales : p.k_bscales) +
-                           ((static_cast<size_t>(pid) * kBS + r) * H_kv + h) * kRowScales;
-      uint8_t* dst = (is_v ? vs_buf(s) : ks_buf(s)) + r * kRowScales;
-      cp_async_n<kRowScales>(dst, src);
-      cp_async_mbar_arrive_noinc(&my_bar[s]);
-    }
     if (lane == x - g_base) {
       const bool bad = cur_pid < 0 || cur_pid >= p.num_blocks;
       const bool need_q = (cur_blk == 0) || (x == t_begin);
       const int n_valid = min(kBS, cur_len - cur_blk * kBS);
       my_info[s] = n_valid | (bad ? 0x100 : 0);
       if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
-      const uint32_t bytes = 2 * kTile + (need_q ? Geo::Q_BYTES : 0);
+      const uint32_t bytes = 2 * kTile + 2 * kScales + (need_q ? Geo::Q_BYTES : 0);
       mbar_arrive_expect_tx(&my_bar[s], bytes);
       const int row = (bad ? 0 : cur_pid) * kBS;
+      if constexpr (Geo::SCALED) {
+        // the unit's scales are one run per block: [kHeads][16][D/16] at unit cur_h
+        const size_t off = (static_cast<size_t>(bad ? 0 : cur_pid) * H_kv + cur_h) * kScales;
+        bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
+        bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
+      }
       if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
         tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
         tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);

@@ -17,6 +17,9 @@
 //    share the request's block table) in one launch -- the request-level transfer of a whole
 //    model; layer-by-layer streaming (page on goodput and PD disaggregation, sec. 5.4, layer
 //    granularity; page "Disaggregated LLM Serving", sec. 5.6) issues one layer at a time.
+//  * the same three moves for the E4M3 block scales of an NVFP4 cache (page "From
+//    PagedAttention to Prefill-Decode disaggregation", sec. 6.2), whose per-block head-major
+//    layout differs from the token-major K/V rows.
 #include "pda_device.cuh"
 #include "pda_internal.h"
 
@@ -141,6 +144,91 @@ __global__ void __launch_bounds__(256) kv_blocks_kernel(const __grid_constant__ 
   }
 }
 
+// ---- NVFP4 block scales: [num_blocks, H_kv, block_size, D/16] E4M3 bytes, per block and
+// head-major, so a (block, kv-head) tile's scales are one contiguous run (what the attention
+// kernel fetches in one bulk copy). The row of (block, offset, head) is
+// (block * H_kv + head) * block_size + offset; these calls move rows of D/16 bytes as
+// 4-byte words (rw words a row).
+struct ScaleJob {
+  uint32_t* buf;  // [len, 2, H_kv, D/16] (pack: written, unpack: read)
+  const int32_t* table;
+  int len;
+};
+
+template <int N>
+struct ScaleParams {
+  int32_t* error_word;
+  uint32_t* k_scales;
+  uint32_t* v_scales;
+  int n, H_kv, rw, block_size, num_blocks;
+  ScaleJob jobs[N];
+};
+
+__device__ __forceinline__ size_t scale_word(long long block, int offset, int h, int H_kv,
+                                             int block_size, int rw, int w) {
+  return (static_cast<size_t>(block * H_kv + h) * block_size + offset) * rw + w;
+}
+
+// Append: k_new/v_new [B, H_kv, D/16]; thread i copies word i of the flattened
+// (b, K|V, head, word) space into the row of slot slot_mapping[b].
+__global__ void __launch_bounds__(256) kv_append_scales_kernel(
+    const uint32_t* __restrict__ k_new, const uint32_t* __restrict__ v_new,
+    uint32_t* __restrict__ k_scales, uint32_t* __restrict__ v_scales,
+    const int32_t* __restrict__ slots, int B, int H_kv, int rw, int block_size, int num_blocks,
+    int32_t* error_word) {
+  const int per = H_kv * rw;
+  const long long total = static_cast<long long>(B) * 2 * per;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(i / (2 * per));
+    const int rem = static_cast<int>(i % (2 * per));
+    const int which = rem / per;
+    const int hw = rem % per;
+    const int s = slots[b];
+    if (s < 0) continue;  // padding
+    const long long block = s / block_size;
+    if (block >= num_blocks) {
+      if (rem == 0) atomic_or_error(error_word, PDA_DEVERR_SLOT);
+      continue;
+    }
+    const size_t dst = scale_word(block, s % block_size, hw / rw, H_kv, block_size, rw, hw % rw);
+    const size_t src = static_cast<size_t>(b) * per + hw;
+    if (which == 0)
+      k_scales[dst] = k_new[src];
+    else
+      v_scales[dst] = v_new[src];
+  }
+}
+
+// Pack (scale rows -> [len, 2, H_kv, D/16]) or unpack (the reverse); blockIdx.y selects the
+// request, threads stride over the buffer's words in order. A block id out of range sets
+// PDA_DEVERR_BLOCK_ID; pack writes 0xFF bytes for its tokens, unpack skips them.
+template <bool kUnpack, int N>
+__global__ void __launch_bounds__(256) kv_scales_kernel(const __grid_constant__ ScaleParams<N> p) {
+  const ScaleJob job = p.jobs[blockIdx.y];
+  const int per = p.H_kv * p.rw;
+  const long long total = static_cast<long long>(job.len) * 2 * per;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / (2 * per));
+    const int rem = static_cast<int>(i % (2 * per));
+    const int which = rem / per;
+    const int hw = rem % per;
+    const int block = job.table[t / p.block_size];
+    const bool bad = block < 0 || block >= p.num_blocks;
+    if (bad && rem == 0) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+    uint32_t* cache = which == 0 ? p.k_scales : p.v_scales;
+    const size_t at =
+        scale_word(bad ? 0 : block, t % p.block_size, hw / p.rw, p.H_kv, p.block_size, p.rw,
+                   hw % p.rw);
+    if (kUnpack) {
+      if (!bad) cache[at] = job.buf[i];
+    } else {
+      job.buf[i] = bad ? 0xffffffffu : cache[at];
+    }
+  }
+}
+
 namespace {
 
 pda_status check_kv_rows(int H_kv, int D, int block_size, int num_blocks, pda_dtype dt,
@@ -244,6 +332,63 @@ pda_status blocks_layers(void* const* bufs, void* const* k_caches, void* const* 
   return launch_blocks(p, context_len, unpack, stream);
 }
 
+
+// Scale rows: D/16 bytes, moved as 4-byte words.
+pda_status check_scale_rows(int H_kv, int D, int block_size, int num_blocks, int* rw) {
+  if (H_kv <= 0 || D <= 0 || block_size <= 0 || num_blocks <= 0) return PDA_ERR_INVALID_ARG;
+  if (D % 64 != 0) return PDA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return PDA_ERR_UNSUPPORTED;
+  *rw = D / 64;
+  return PDA_OK;
+}
+
+pda_status scales_batched(void* const* bufs, const int32_t* const* block_table_rows,
+                          const int32_t* context_lens, int n, const void* k_scales,
+                          const void* v_scales, int H_kv, int D, int block_size, int num_blocks,
+                          int32_t* error_word, bool unpack, cudaStream_t stream) {
+  if (n < 0 || n > PDA_PACK_MAX_BATCH) return n < 0 ? PDA_ERR_INVALID_ARG : PDA_ERR_UNSUPPORTED;
+  int rw = 0;
+  const pda_status st = check_scale_rows(H_kv, D, block_size, num_blocks, &rw);
+  if (st != PDA_OK) return st;
+  if (n == 0) return PDA_OK;
+  if (bufs == nullptr || block_table_rows == nullptr || context_lens == nullptr ||
+      k_scales == nullptr || v_scales == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned4(k_scales) || !aligned4(v_scales)) return PDA_ERR_INVALID_ARG;
+  ScaleParams<PDA_PACK_MAX_BATCH> p;
+  p.error_word = error_word;
+  p.k_scales = static_cast<uint32_t*>(const_cast<void*>(k_scales));
+  p.v_scales = static_cast<uint32_t*>(const_cast<void*>(v_scales));
+  p.H_kv = H_kv;
+  p.rw = rw;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  int m = 0, max_len = 0;
+  for (int i = 0; i < n; ++i) {
+    const int len = context_lens[i];
+    if (len < 0) return PDA_ERR_INVALID_ARG;
+    if (len == 0) continue;
+    if (bufs[i] == nullptr || block_table_rows[i] == nullptr || !aligned4(bufs[i]))
+      return PDA_ERR_INVALID_ARG;
+    p.jobs[m].buf = static_cast<uint32_t*>(bufs[i]);
+    p.jobs[m].table = block_table_rows[i];
+    p.jobs[m].len = len;
+    if (len > max_len) max_len = len;
+    ++m;
+  }
+  if (m == 0) return PDA_OK;
+  p.n = m;
+  const long long words = static_cast<long long>(max_len) * 2 * H_kv * rw;
+  long long gx = (words + 255) / 256;
+  if (gx > 4096) gx = 4096;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(m));
+  if (unpack)
+    kv_scales_kernel<true, PDA_PACK_MAX_BATCH><<<grid, 256, 0, stream>>>(p);
+  else
+    kv_scales_kernel<false, PDA_PACK_MAX_BATCH><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pda
 
@@ -341,4 +486,46 @@ extern "C" pda_status pda_kv_unpack_blocks(const void* in, void* k_cache, void* 
   const int32_t lens[1] = {context_len};
   return pda_kv_unpack_blocks_batched(ins, rows, lens, 1, k_cache, v_cache, H_kv, D,
                                       block_size, num_blocks, kv_dtype, error_word, stream);
+}
+
+extern "C" pda_status pda_kv_append_block_scales(const void* k_new, const void* v_new,
+                                                 void* k_scales, void* v_scales,
+                                                 const int32_t* slot_mapping, int B, int H_kv,
+                                                 int D, int block_size, int num_blocks,
+                                                 int32_t* error_word, cudaStream_t stream) {
+  if (B < 0) return PDA_ERR_INVALID_ARG;
+  int rw = 0;
+  const pda_status st = check_scale_rows(H_kv, D, block_size, num_blocks, &rw);
+  if (st != PDA_OK) return st;
+  if (B == 0) return PDA_OK;
+  if (k_new == nullptr || v_new == nullptr || k_scales == nullptr || v_scales == nullptr ||
+      slot_mapping == nullptr)
+    return PDA_ERR_INVALID_ARG;
+  if (!aligned4(k_new) || !aligned4(v_new) || !aligned4(k_scales) || !aligned4(v_scales))
+    return PDA_ERR_INVALID_ARG;
+  const long long total = static_cast<long long>(B) * 2 * H_kv * rw;
+  long long grid = (total + 255) / 256;
+  if (grid > 65535) grid = 65535;
+  kv_append_scales_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const uint32_t*>(k_new), static_cast<const uint32_t*>(v_new),
+      static_cast<uint32_t*>(k_scales), static_cast<uint32_t*>(v_scales), slot_mapping, B, H_kv,
+      rw, block_size, num_blocks, error_word);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
+extern "C" pda_status pda_kv_pack_block_scales_batched(
+    void* const* outs, const int32_t* const* block_table_rows, const int32_t* context_lens,
+    int n, const void* k_scales, const void* v_scales, int H_kv, int D, int block_size,
+    int num_blocks, int32_t* error_word, cudaStream_t stream) {
+  return scales_batched(outs, block_table_rows, context_lens, n, k_scales, v_scales, H_kv, D,
+                        block_size, num_blocks, error_word, false, stream);
+}
+
+extern "C" pda_status pda_kv_unpack_block_scales_batched(
+    const void* const* ins, const int32_t* const* block_table_rows, const int32_t* context_lens,
+    int n, void* k_scales, void* v_scales, int H_kv, int D, int block_size, int num_blocks,
+    int32_t* error_word, cudaStream_t stream) {
+  return scales_batched(const_cast<void* const*>(ins), block_table_rows, context_lens, n,
+                        k_scales, v_scales, H_kv, D, block_size, num_blocks, error_word, true,
+                        stream);
 }

@@ -124,20 +124,6 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
                "l"(reinterpret_cast<uint64_t>(src))
                : "memory");
 }
-// cp.async of `bytes` (4, 8 or 16, both addresses aligned to it) global -> shared.
-template <int bytes>
-__device__ __forceinline__ void cp_async_n(void* dst, const void* src) {
-  static_assert(bytes == 4 || bytes == 8 || bytes == 16, "cp.async sizes");
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst)),
-               "l"(reinterpret_cast<uint64_t>(src)), "n"(bytes)
-               : "memory");
-}
-// When all of this thread's earlier cp.async copies have landed, performs one arrive on
-// `bar` (counted in the barrier's initial arrival count: no pending increment).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

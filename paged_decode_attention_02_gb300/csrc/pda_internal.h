@@ -38,6 +38,7 @@ inline bool dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16 || t == PDA_F
 // Types of q and out.
 inline bool float_dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace pda

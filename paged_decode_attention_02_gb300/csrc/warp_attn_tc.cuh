@@ -407,7 +407,7 @@ struct WarpAttnTC {
 };
 
 // Two adjacent kv-heads A (tile bytes [0, TILE_BYTES)) and B ([TILE_BYTES, 2 TILE_BYTES)) per
-// tile, GH <= 4 query heads each. Unit head j: A's local j for j < GH, B's local j - GH
+// tile, GH <= 4 query heads each; NVFP4 scales likewise, A's [16][D/16] then B's. Unit head j: A's local j for j < GH, B's local j - GH
 // otherwise (the q rows and output rows of the unit are in that order). Lane g holds head
 // A_g's and B_g's scores (separate accumulators) and running state; the shared O^T holds
 // A's heads in columns 0..GH-1 and B's in 4..4+GH-1: the PV products of head A get P^T
@@ -419,7 +419,7 @@ struct WarpAttnTCPair {
   using Ops = TCOps<KV, D>;
   static constexpr int G = 2 * GH;                 // query heads of the unit
   static constexpr int ROW_SCALES = D / 16;        // NVFP4 scale bytes per row and head
-  static constexpr int SCALE_STRIDE = 2 * ROW_SCALES;  // unit scale row: A's then B's
+  static constexpr int HEAD_SCALES = 16 * ROW_SCALES;  // a head's tile of scales: A's, B's
 
   int g, t4;
   uint32_t qa[2][8][2];  // q of heads A_g, B_g as A fragments
@@ -463,7 +463,7 @@ struct WarpAttnTCPair {
     float sc[2][2][4] = {};  // head, n-tile
 #pragma unroll
     for (int u = 0; u < 2; ++u)
-      Ops::qk(sc[u], qa[u], ks + u * Ops::TILE_BYTES, ksc + u * ROW_SCALES, SCALE_STRIDE, g,
+      Ops::qk(sc[u], qa[u], ks + u * Ops::TILE_BYTES, ksc + u * HEAD_SCALES, ROW_SCALES, g,
               t4);
     float x[2][4];
     float alpha[2];
@@ -517,9 +517,9 @@ struct WarpAttnTCPair {
     }
     uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
     if (kPartial) Ops::keep_masks(t4, n_valid, keep_lo, keep_hi);
-    Ops::pv(o, vs, vsc, SCALE_STRIDE, v_off, g, t4, pA[0], pA[1], pA[2], pA[3], keep_lo,
+    Ops::pv(o, vs, vsc, ROW_SCALES, v_off, g, t4, pA[0], pA[1], pA[2], pA[3], keep_lo,
             keep_hi);
-    Ops::pv(o, vs + Ops::TILE_BYTES, vsc + ROW_SCALES, SCALE_STRIDE, v_off, g, t4, pB[0],
+    Ops::pv(o, vs + Ops::TILE_BYTES, vsc + HEAD_SCALES, ROW_SCALES, v_off, g, t4, pB[0],
             pB[1], pB[2], pB[3], keep_lo, keep_hi);
   }
 

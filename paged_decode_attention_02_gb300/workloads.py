@@ -24,7 +24,8 @@ Recipe (one per named workload):
     torch's float8_e4m3fn rounding), drawn with the seeds of their bf16 twin so the
     lengths and tables are the same;
   - NVFP4 workloads store random E2M1 code bytes and random E4M3 block scales in
-    [0.25, 0.47) (per-tensor scales 0.9 for K, 1.3 for V), also on their twin's seeds;
+    [0.25, 0.47) (per-tensor scales 0.9 for K, 1.3 for V), also on their twin's seeds; the
+    cache's scales are laid out [num_blocks, H_kv, block_size, D/16];
   - context lengths count the tokens after this step's append, so the appended token is
     the last position each request attends to; ``slot_mapping[b]`` points at it.
 """
@@ -185,7 +186,8 @@ class Step:
     pack_requests: list
     k_scale: float = 1.0
     v_scale: float = 1.0
-    # NVFP4: block scales of the caches and of the new tokens ([..., H_kv, D/16] E4M3 bytes);
+    # NVFP4: block scales of the caches ([NB, H_kv, bs, D/16] E4M3 bytes, per block and
+    # head-major) and of the new tokens ([B, H_kv, D/16]);
     # k_cache / v_cache / k_new / v_new then hold the packed E2M1 codes ([..., H_kv, D/2])
     k_bscales: torch.Tensor | None = None
     v_bscales: torch.Tensor | None = None
@@ -269,7 +271,9 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
         v_cache = codes((NB, bs, w.H_kv, half))
         k_new = codes((B, w.H_kv, half))
         v_new = codes((B, w.H_kv, half))
-        nv = dict(k_bscales=bscales((NB, bs, w.H_kv, nsc)), v_bscales=bscales((NB, bs, w.H_kv, nsc)),
+        # cache scales per block, head-major: [NB, H_kv, bs, D/16]
+        nv = dict(k_bscales=bscales((NB, w.H_kv, bs, nsc)),
+                  v_bscales=bscales((NB, w.H_kv, bs, nsc)),
                   k_new_bscales=bscales((B, w.H_kv, nsc)), v_new_bscales=bscales((B, w.H_kv, nsc)))
     elif w.kv == "fp8":
         # N(0,1) values stored as E4M3 codes of value / scale (round to nearest even)
@@ -293,8 +297,8 @@ def make_step(w: Workload | str, device="cpu", B: int | None = None, seed: int |
         bad = torch.from_numpy(~valid).to(device).view(NB, bs)
         nan = 0x7F if w.kv == "fp8" else float("nan")  # 0x7F is the E4M3 NaN code
         if w.kv == "nvfp4":  # E2M1 has no NaN: poison the rows' block scales instead
-            nv["k_bscales"][bad] = 0x7F
-            nv["v_bscales"][bad] = 0x7F
+            nv["k_bscales"].permute(0, 2, 1, 3)[bad] = 0x7F
+            nv["v_bscales"].permute(0, 2, 1, 3)[bad] = 0x7F
         else:
             k_cache[bad] = nan
             v_cache[bad] = nan

@@ -67,7 +67,7 @@ def _oracle_attention(s, q, kc, vc, bt, lens, ksc=None, vsc=None, num_threads=0)
 
 def oracle_full_step(s, append: bool = True, num_threads: int = 0):
     """fp64 oracle of the whole step on host copies taken before the GPU runs. For NVFP4
-    the block-scale tensors are appended like the data (both are byte caches)."""
+    the new tokens' block scales are appended into the per-block scale caches as well."""
     kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
     ksc = vsc = None
     if s.w.kv == "nvfp4":
@@ -75,8 +75,8 @@ def oracle_full_step(s, append: bool = True, num_threads: int = 0):
     if append:
         assert orc.kv_append(to_np(s.k_new), to_np(s.v_new), kc, vc, s.slot_mapping_np) == 0
         if ksc is not None:
-            assert orc.kv_append(to_np(s.k_new_bscales), to_np(s.v_new_bscales), ksc, vsc,
-                                 s.slot_mapping_np) == 0
+            assert orc.kv_append_block_scales(to_np(s.k_new_bscales), to_np(s.v_new_bscales),
+                                              ksc, vsc, s.slot_mapping_np) == 0
     ref, st = _oracle_attention(s, to_np(s.q), kc, vc, s.block_tables_np, s.context_lens_np,
                                 ksc, vsc, num_threads)
     return ref, st, kc, vc
@@ -112,8 +112,8 @@ def oracle_sampled(s, reqs, append: bool = True):
         st = orc.kv_append(to_np(s.k_new[reqs]), to_np(s.v_new[reqs]), kc, vc, slots)
         assert st == 0
         if ksc is not None:
-            st = orc.kv_append(to_np(s.k_new_bscales[reqs]), to_np(s.v_new_bscales[reqs]), ksc,
-                               vsc, slots)
+            st = orc.kv_append_block_scales(to_np(s.k_new_bscales[reqs]),
+                                            to_np(s.v_new_bscales[reqs]), ksc, vsc, slots)
             assert st == 0
     return _oracle_attention(s, to_np(s.q[reqs]).copy(), kc, vc, bt, lens, ksc, vsc)
 
@@ -124,8 +124,8 @@ def gpu_step(s, append: bool = True, sm_cap: int = 0, out_dtype=None, workspace=
     if append:
         pda.kv_append(s.k_new, s.v_new, s.k_cache, s.v_cache, s.slot_mapping, error_word=err)
         if s.w.kv == "nvfp4":
-            pda.kv_append(s.k_new_bscales, s.v_new_bscales, s.k_bscales, s.v_bscales,
-                          s.slot_mapping, error_word=err)
+            pda.kv_append_block_scales(s.k_new_bscales, s.v_new_bscales, s.k_bscales,
+                                       s.v_bscales, s.slot_mapping, error_word=err)
     out = torch.empty(s.q.shape, dtype=out_dtype or s.q.dtype, device=s.q.device)
     if s.w.kv == "nvfp4":
         pda.paged_decode_attention_nvfp4(out, s.q, s.k_cache, s.v_cache, s.k_bscales,

@@ -498,14 +498,15 @@ def test_nvfp4_shapes_and_groups(D, H, H_kv):
     w = variant("llama2_13b_b80_nvfp4", D=D, H=H, H_kv=H_kv, B=9, lengths="uniform:1,700")
     lens = np.array([1, 15, 16, 17, 31, 32, 33, 700, 255], np.int32)
     s = wl.make_step(w, device=DEV, lengths=lens)
-    # the byte append needs 16-byte rows: H_kv * D / 16 scale bytes (odd H_kv at D = 128
-    # gives 8-byte multiples), so those shapes test the attention alone
-    append = (H_kv * D // 16) % 16 == 0
-    ref, st, kc, vc = oracle_full_step(s, append=append)
+    ksc, vsc = to_np(s.k_bscales).copy(), to_np(s.v_bscales).copy()
+    assert orc.kv_append_block_scales(to_np(s.k_new_bscales), to_np(s.v_new_bscales), ksc, vsc,
+                                      s.slot_mapping_np) == 0
+    ref, st, kc, vc = oracle_full_step(s)
     assert st == 0
-    out, err = gpu_step(s, append=append)
+    out, err = gpu_step(s)
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
+    assert np.array_equal(to_np(s.k_bscales), ksc) and np.array_equal(to_np(s.v_bscales), vsc)
     assert_attention_close(out, ref, f"nvfp4 D={D} H={H} H_kv={H_kv}")
 
 
@@ -542,17 +543,89 @@ def test_nvfp4_empty_single_and_poisoned_scales():
 
 def test_nvfp4_pack_of_data_and_scales_is_bit_exact():
     s = wl.make_step("gqa_skew_b256_nvfp4", device=DEV, B=8)
-    r = int(np.argmax(s.context_lens_np))
-    L = int(s.context_lens_np[r])
-    n = (L + 15) // 16
-    blocks = torch.from_numpy(s.block_tables_np[r, :n].astype(np.int64)).to(DEV)
-    for data_k, data_v in ((s.k_cache, s.v_cache), (s.k_bscales, s.v_bscales)):
-        packed = torch.empty((L, 2) + tuple(data_k.shape[2:]), dtype=torch.uint8, device=DEV)
-        pda.kv_pack_blocks(packed, data_k, data_v, s.block_tables[r], L)
-        want, st = orc.kv_pack_blocks(to_np(data_k.index_select(0, blocks)).copy(),
-                                      to_np(data_v.index_select(0, blocks)).copy(),
-                                      np.arange(n, dtype=np.int32), L)
-        assert st == 0 and np.array_equal(to_np(packed), want)
+    reqs = [int(r) for r in np.argsort(-s.context_lens_np)[:4]]
+    lens = [int(s.context_lens_np[r]) for r in reqs]
+    rows = [s.block_tables[r] for r in reqs]
+    kd, vd = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
+    ksc, vsc = to_np(s.k_bscales).copy(), to_np(s.v_bscales).copy()
+    data = [torch.empty((L, 2, s.w.H_kv, s.w.D // 2), dtype=torch.uint8, device=DEV)
+            for L in lens]
+    scales = [torch.empty((L, 2, s.w.H_kv, s.w.D // 16), dtype=torch.uint8, device=DEV)
+              for L in lens]
+    pda.kv_pack_blocks_batched(data, s.k_cache, s.v_cache, rows, lens)
+    pda.kv_pack_block_scales_batched(scales, s.k_bscales, s.v_bscales, rows, lens)
+    for i, r in enumerate(reqs):
+        want, st = orc.kv_pack_blocks(kd, vd, s.block_tables_np[r], lens[i])
+        assert st == 0 and np.array_equal(to_np(data[i]), want), r
+        want, st = orc.kv_pack_block_scales(ksc, vsc, s.block_tables_np[r], lens[i])
+        assert st == 0 and np.array_equal(to_np(scales[i]), want), r
+
+
+def test_nvfp4_unpack_scales_inverts_pack_and_touches_nothing_else():
+    s = wl.make_step("llama2_13b_b80_nvfp4", device=DEV, B=5)
+    reqs = list(range(s.B))
+    lens = [int(s.context_lens_np[r]) for r in reqs]
+    rows = [s.block_tables[r] for r in reqs]
+    packed = [torch.from_numpy(orc.kv_pack_block_scales(to_np(s.k_bscales), to_np(s.v_bscales),
+                                                        s.block_tables_np[r], L)[0]).to(DEV)
+              for r, L in zip(reqs, lens)]
+    k2 = torch.full_like(s.k_bscales, 0x5A)
+    v2 = torch.full_like(s.v_bscales, 0xA5)
+    kw, vw = to_np(k2).copy(), to_np(v2).copy()
+    for r, L, p in zip(reqs, lens, packed):
+        assert orc.kv_unpack_block_scales(to_np(p), kw, vw, s.block_tables_np[r], L) == 0
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_unpack_block_scales_batched(packed, k2, v2, rows, lens, error_word=err)
+    assert int(err.item()) == 0
+    assert np.array_equal(to_np(k2), kw) and np.array_equal(to_np(v2), vw)
+
+
+def test_nvfp4_scale_calls_edge_cases():
+    """Padding and out-of-range slots in the scale append; a bad block id in the scale pack
+    (0xFF for its tokens) and unpack (not written); empty requests; D not a multiple of 64."""
+    s = wl.make_step("llama2_13b_b80_nvfp4", device=DEV, B=4)
+    slots = s.slot_mapping.clone()
+    slots[1] = -1
+    slots[2] = s.num_blocks * s.w.block_size + 5
+    ksc, vsc = to_np(s.k_bscales).copy(), to_np(s.v_bscales).copy()
+    assert orc.kv_append_block_scales(to_np(s.k_new_bscales), to_np(s.v_new_bscales), ksc, vsc,
+                                      to_np(slots)) != 0  # the oracle flags slot 2 too
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pda.kv_append_block_scales(s.k_new_bscales, s.v_new_bscales, s.k_bscales, s.v_bscales,
+                               slots, error_word=err)
+    assert int(err.item()) == binding.PDA_DEVERR_SLOT
+    assert np.array_equal(to_np(s.k_bscales), ksc) and np.array_equal(to_np(s.v_bscales), vsc)
+
+    L = int(s.context_lens_np[0])
+    row = s.block_tables[0].clone()
+    row[0] = s.num_blocks + 7
+    out = torch.zeros((L, 2, s.w.H_kv, s.w.D // 16), dtype=torch.uint8, device=DEV)
+    err.zero_()
+    pda.kv_pack_block_scales_batched([out], s.k_bscales, s.v_bscales, [row], [L], error_word=err)
+    assert int(err.item()) == binding.PDA_DEVERR_BLOCK_ID
+    n0 = min(L, s.w.block_size)
+    assert (out[:n0] == 0xFF).all()
+    want, st = orc.kv_pack_block_scales(ksc, vsc, s.block_tables_np[0], L)
+    assert st == 0 and np.array_equal(to_np(out[n0:]), want[n0:])
+
+    k2, v2 = torch.zeros_like(s.k_bscales), torch.zeros_like(s.v_bscales)
+    err.zero_()
+    pda.kv_unpack_block_scales_batched([out], k2, v2, [row], [L], error_word=err)
+    assert int(err.item()) == binding.PDA_DEVERR_BLOCK_ID
+    kw, vw = np.zeros_like(ksc), np.zeros_like(vsc)
+    bad_row = s.block_tables_np[0].copy()
+    bad_row[0] = s.num_blocks + 7
+    assert orc.kv_unpack_block_scales(to_np(out), kw, vw, bad_row, L) != 0
+    assert np.array_equal(to_np(k2), kw) and np.array_equal(to_np(v2), vw)
+
+    pda.kv_pack_block_scales_batched([out], s.k_bscales, s.v_bscales, [row], [0])  # no-op
+    pda.kv_pack_block_scales_batched([], s.k_bscales, s.v_bscales, [], [])
+    odd = torch.zeros((s.num_blocks, s.w.H_kv, s.w.block_size, 2), dtype=torch.uint8,
+                      device=DEV)  # D = 32
+    with pytest.raises(binding.PdaError) as e:
+        pda.kv_pack_block_scales_batched([out[:, :, :, :2].contiguous()], odd, odd,
+                                         [s.block_tables[0]], [L])
+    assert e.value.status == binding.PDA_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------------ tensor-core tile step

@@ -19,6 +19,18 @@ def test_nvfp4_workload_has_codes_and_block_scales():
     assert s.k_cache.shape[-1] == w.D // 2 and s.k_bscales.shape[-1] == w.D // 16
     assert s.k_new.shape == (2, w.H_kv, w.D // 2) and s.k_new_bscales.shape == (2, w.H_kv, w.D // 16)
     assert int(s.k_bscales.min()) >= 0x28 and int(s.k_bscales.max()) < 0x30
+    assert s.k_bscales.shape == (s.num_blocks, w.H_kv, w.block_size, w.D // 16)
+
+
+def test_nvfp4_poison_marks_unused_rows_in_head_major_scales():
+    s = wl.make_step("llama2_13b_b80_nvfp4", B=2, poison_unused=True)
+    bs = s.w.block_size
+    used = np.zeros((s.num_blocks, bs), bool)
+    for b in range(s.B):
+        for t in range(int(s.context_lens_np[b])):
+            used[s.block_tables_np[b, t // bs], t % bs] = True
+    nan_rows = (s.k_bscales == 0x7F).all(dim=-1).all(dim=1).cpu().numpy()  # [NB, bs]
+    assert np.array_equal(nan_rows, ~used)
 
 
 def test_fp8_workload_shares_lengths_and_tables_with_its_twin():
