@@ -83,6 +83,7 @@ def hbm_peak():
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
+    h.update(os.environ.get("PDA_NVCC_DEFINES", "").encode())  # build options change the code
     for p in ATTN_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
@@ -239,6 +240,18 @@ def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def arith_dtype(w) -> str:
+    """The arithmetic type of the attention: at D = 128 the tensor cores multiply bf16
+    operands (bf16 caches) or fp16 ones (exact quantised codes) into fp32, with the
+    probabilities split in two parts; fp32 caches and D = 64 run fp32 on the CUDA cores."""
+    if w.D == 128 and w.kv:
+        return "f16 mma, f32 accumulate"
+    if w.D == 128 and w.dtype == "bf16" and "PDA_BF16_TC=0" not in os.environ.get(
+            "PDA_NVCC_DEFINES", ""):
+        return "bf16 mma, f32 accumulate"
+    return "f32"
 
 
 def kv_arrays(s):
@@ -496,9 +509,7 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        # arithmetic type: fp32 on the CUDA cores; quantised caches at D = 128 multiply fp16
-        # operands (exact codes, split probabilities) on the tensor cores into fp32
-        "dtype": "f16 mma, f32 accumulate" if (w.kv and w.D == 128) else "f32",
+        "dtype": arith_dtype(w),
         "data": "synthetic",
         "config": {"workload": w.name, "B": s.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
                    "block_size": w.block_size, "kv_dtype": w.kv or w.dtype,

@@ -30,6 +30,12 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+def _defines():
+    """Extra -D options from PDA_NVCC_DEFINES (space-separated NAME=VALUE), for tuning builds
+    (the csrc macros PDA_ATTN_WARPS, PDA_TC_PAIR_WARPS_*, PDA_BF16_TC, ...)."""
+    return ["-D" + d for d in os.environ.get("PDA_NVCC_DEFINES", "").split() if d]
+
+
 def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
@@ -54,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *_defines(), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
