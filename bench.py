@@ -242,18 +242,6 @@ def barrier(ws):
         dist.barrier()
 
 
-def arith_dtype(w) -> str:
-    """The arithmetic type of the attention: at D = 128 the tensor cores multiply bf16
-    operands (bf16 caches) or fp16 ones (exact quantised codes) into fp32, with the
-    probabilities split in two parts; fp32 caches and D = 64 run fp32 on the CUDA cores."""
-    if w.D == 128 and w.kv:
-        return "f16 mma, f32 accumulate"
-    if w.D == 128 and w.dtype == "bf16" and "PDA_BF16_TC=0" not in os.environ.get(
-            "PDA_NVCC_DEFINES", ""):
-        return "bf16 mma, f32 accumulate"
-    return "f32"
-
-
 def kv_arrays(s):
     """Per stored array pair of a step: (cache K, cache V, new K, new V, append, batched pack,
     batched unpack) -- the K/V rows, and for NVFP4 also the block scales, which have their
@@ -509,7 +497,9 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": arith_dtype(w),
+        # arithmetic type: fp32 on the CUDA cores; quantised caches at D = 128 multiply fp16
+        # operands (exact codes, split probabilities) on the tensor cores into fp32
+        "dtype": "f16 mma, f32 accumulate" if (w.kv and w.D == 128) else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": s.B, "H": w.H, "H_kv": w.H_kv, "D": w.D,
                    "block_size": w.block_size, "kv_dtype": w.kv or w.dtype,

@@ -32,7 +32,7 @@ def _nvcc() -> str:
 
 def _defines():
     """Extra -D options from PDA_NVCC_DEFINES (space-separated NAME=VALUE), for tuning builds
-    (the csrc macros PDA_ATTN_WARPS, PDA_TC_PAIR_WARPS_*, PDA_BF16_TC, ...)."""
+    (the csrc macros PDA_ATTN_WARPS, PDA_TC_PAIR_WARPS_*, PDA_PACK_TOKENS, ...)."""
     return ["-D" + d for d in os.environ.get("PDA_NVCC_DEFINES", "").split() if d]
 
 

@@ -27,14 +27,13 @@
 //    with a log-sum-exp combine, so no second kernel is needed. This is the split and merge
 //    of Orca's iteration-level batching (page "Disaggregated LLM Serving", sec. 2.1),
 //    applied along the sequence.
-//  * At D = 128 the dot products of bf16 and quantised (FP8, NVFP4) caches run on the
-//    tensor cores (warp_attn_tc.cuh), mostly on units of two adjacent kv-heads (one TMA
-//    box for both): bf16 K and V are mma operands as stored, so a tile costs a fraction of
-//    the CUDA-core step's instructions (what an SM-capped launch is limited by), and the
-//    quantised caches carry two to four times as many tokens per byte. fp32 caches, D = 64
-//    and single-head G = 1 tiles run on the CUDA cores (G dot products of length D per
-//    token). The pipeline, scheduling and merge below are shared and see a pair as one
-//    unit with 2 G query heads.
+//  * bf16 and fp32 caches run on the CUDA cores: per kv-head and token this is G dot
+//    products of length D against 2 * D * sizeof(elem) bytes, and the bf16 path already
+//    streams at the HBM rate. Quantised caches (FP8, NVFP4) at D = 128 carry two to four
+//    times as many tokens per byte, so their dot products go to the tensor cores
+//    (warp_attn_tc.cuh), mostly on units of two adjacent kv-heads (one TMA box for both);
+//    the pipeline, scheduling and merge below are shared and see a pair as one unit with
+//    2 G query heads.
 #include <math.h>
 
 #include <atomic>
@@ -55,10 +54,6 @@ namespace pda {
 #endif
 #ifndef PDA_ATTN_MAX_STAGES
 #define PDA_ATTN_MAX_STAGES 4  // most pipeline stages per warp
-#endif
-
-#ifndef PDA_BF16_TC
-#define PDA_BF16_TC 1          // bf16 caches at D = 128 on the tensor cores (0: CUDA cores)
 #endif
 
 #ifndef PDA_TC_WARPS
@@ -84,24 +79,11 @@ __host__ __device__ constexpr int warps_for_group(int G, bool tc) {
 #ifndef PDA_TC_PAIR_WARPS_NVFP4
 #define PDA_TC_PAIR_WARPS_NVFP4 12
 #endif
-#ifndef PDA_TC_PAIR_WARPS_BF16
-#define PDA_TC_PAIR_WARPS_BF16 8
-#endif
-#ifndef PDA_BF16_TC_PAIR
-#define PDA_BF16_TC_PAIR 1     // bf16 pairs of kv-heads per tile where possible (0: one)
-#endif
-static_assert(PDA_TC_PAIR_WARPS_FP8 <= kMaxWarps && PDA_TC_PAIR_WARPS_NVFP4 <= kMaxWarps &&
-                  PDA_TC_PAIR_WARPS_BF16 <= kMaxWarps,
+static_assert(PDA_TC_PAIR_WARPS_FP8 <= kMaxWarps && PDA_TC_PAIR_WARPS_NVFP4 <= kMaxWarps,
               "per-warp shared arrays are sized for kMaxWarps");
-// kv: 0 FP8, 1 NVFP4, 2 bf16 (only the two-head step tells them apart)
-__host__ __device__ constexpr int warps_for_mode(int G, int mode, int kv) {
-  return mode == 2 ? (kv == 1 ? PDA_TC_PAIR_WARPS_NVFP4
-                              : kv == 2 ? PDA_TC_PAIR_WARPS_BF16 : PDA_TC_PAIR_WARPS_FP8)
+__host__ __device__ constexpr int warps_for_mode(int G, int mode, bool fp4) {
+  return mode == 2 ? (fp4 ? PDA_TC_PAIR_WARPS_NVFP4 : PDA_TC_PAIR_WARPS_FP8)
                    : warps_for_group(G, mode != 0);
-}
-template <typename KV>
-constexpr int kv_kind() {
-  return std::is_same<KV, nvfp4>::value ? 1 : std::is_same<KV, __nv_bfloat16>::value ? 2 : 0;
 }
 // Stage alignment: the tensor-core step reads TMA tiles written with the 128-byte (FP8) or
 // 64-byte (NVFP4) swizzle, whose pattern repeats every 1024 (512) bytes.
@@ -412,10 +394,6 @@ struct WarpAttn {
 
 // n fp32 values (n = 2 or a multiple of 4, p aligned to n * 4 bytes up to 16).
 __device__ __forceinline__ void store_f32(float* p, const float* v, int n) {
-  if (n == 1) {
-    *p = v[0];
-    return;
-  }
   if (n == 2) {
     *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
     return;
@@ -582,12 +560,11 @@ __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1,
 // 4-D TMA box). G is the unit's query heads: the kv-head's G, or 2 G for a pair; p.H_kv
 // counts units (kv-heads, or pairs).
 template <typename KV, typename QT, int D, int G, int MODE>
-__global__ void __launch_bounds__(warps_for_mode(G, MODE, kv_kind<KV>()) * 32, 1)
+__global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4>::value) * 32,
+                                  1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   constexpr bool TC = MODE != kModeCuda;
-  // bf16 tensor-core tiles: 256-byte rows, loaded as two swizzled 128-byte halves
-  constexpr bool kSplitRows = TC && std::is_same<KV, __nv_bfloat16>::value;
   using Geo = Geometry<KV, QT, D, G>;
   using W = std::conditional_t<
       MODE == kModeCuda, WarpAttn<KV, QT, D, G>,
@@ -774,15 +751,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, kv_kind<KV>()) * 32, 1
         bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
         bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
       }
-      if constexpr (kSplitRows && MODE == kModeTcPair) {
-        // bf16 rows as two 128-byte halves: K box (d, half, row, head, pair) -> [head][row]
-        // [half]; V box (d, row, half, head, pair) -> [head][half][row]
-        tma_load_5d(k_buf(s), &tmK, 0, 0, row, 0, cur_h, &my_bar[s], policy);
-        tma_load_5d(v_buf(s), &tmV, 0, row, 0, 0, cur_h, &my_bar[s], policy);
-      } else if constexpr (kSplitRows) {  // K (d, half, head, row), V (d, row, half, head)
-        tma_load_4d(k_buf(s), &tmK, 0, 0, cur_h, row, &my_bar[s], policy);
-        tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);
-      } else if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
+      if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
         tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
         tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);
       } else {
@@ -938,23 +907,16 @@ struct Tiling {
   int G_u;    // query heads per unit
 };
 
-// bf16 and quantised caches at D = 128 run on the tensor cores (fp32 caches and D = 64 on
-// the CUDA cores). Where H_kv is even and G <= 4, two adjacent kv-heads share a tile (one
-// TMA box and one pipeline step for both): per byte that halves the TMA operations, which
-// bound small quantised tiles (about one per 120 SM cycles, whatever their size), and the
-// per-tile pipeline work. Otherwise a tile is one kv-head on the tensor cores for G >= 2,
-// and on the CUDA cores for G = 1 (a plain GEMV, where they keep up: measured equal to the
-// single-head tensor-core step for quantised caches). A bf16 launch capped to part of the
-// GPU uses one-kv-head tiles: it is bound by the bytes each SM keeps in flight, and a pair
-// stage (16 KB) is held about twice as long by its compute as a single one (measured at
-// 16 / 31 / 61 SMs: pairs 20.6 / 38.7 / 73.8 % of peak, single tiles 22.3 / 42.0 / 80.4 %,
-// the CUDA-core step 22.4 / 41.9 / 80.4 %; on all SMs pairs are 0-2.5 % faster).
-Tiling tiling_for(pda_dtype kv, int D, int H_kv, int G, bool capped) {
-  const bool tc =
-      (kv == PDA_FP8_E4M3 || kv == PDA_NVFP4 || (kv == PDA_BF16 && PDA_BF16_TC)) && D == 128;
-  const bool pairs = kv != PDA_BF16 || (PDA_BF16_TC_PAIR && !capped);
-  if (tc && pairs && G <= 4 && H_kv % 2 == 0) return {kModeTcPair, H_kv / 2, 2 * G};
-  if (tc && G >= 2) return {kModeTc, H_kv, G};
+// Quantised caches at D = 128 run on the tensor cores. Where H_kv is even and G <= 4, two
+// adjacent kv-heads share a tile (one TMA box and one pipeline step for both): per byte
+// that halves the TMA operations, which bound small quantised tiles (about one per 120 SM
+// cycles, whatever their size), and the per-tile pipeline work. Otherwise a quantised tile
+// is one kv-head on the tensor cores for G >= 2, and on the CUDA cores for G = 1 (a plain
+// GEMV, where they keep up: measured equal to the single-head tensor-core step).
+Tiling tiling_for(pda_dtype kv, int D, int H_kv, int G) {
+  const bool quantised = kv == PDA_FP8_E4M3 || kv == PDA_NVFP4;
+  if (quantised && D == 128 && G <= 4 && H_kv % 2 == 0) return {kModeTcPair, H_kv / 2, 2 * G};
+  if (quantised && D == 128 && G >= 2) return {kModeTc, H_kv, G};
   return {kModeCuda, H_kv, G};
 }
 
@@ -968,12 +930,9 @@ uint32_t stage_bytes_for(pda_dtype kv, int D, const Tiling& t) {
       round_up(2 * tile + scales + q, stage_align(t.mode != kModeCuda)));
 }
 
-// A launch on fewer than all SMs is capped: it is bound by the bytes each SM keeps in flight.
-bool is_capped(int sm_cap, int num_sms) { return sm_cap > 0 && sm_cap < num_sms; }
-
 bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
                LaunchPlan* pl) {
-  const Tiling t = tiling_for(kv, D, H_kv, G, is_capped(sm_cap, num_sms));
+  const Tiling t = tiling_for(kv, D, H_kv, G);
   const bool tc = t.mode != kModeCuda;
   const size_t align = stage_align(tc);
   pl->stage_bytes = stage_bytes_for(kv, D, t);
@@ -983,8 +942,7 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
   if (fixed >= static_cast<size_t>(kSmemBudget)) return false;
   pl->nwarps = 0;
   // The most warps that still get two stages each; then as many stages as fit.
-  const int kind = kv == PDA_NVFP4 ? 1 : kv == PDA_BF16 ? 2 : 0;
-  for (int nw = warps_for_mode(t.G_u, t.mode, kind); nw >= 2; --nw) {
+  for (int nw = warps_for_mode(t.G_u, t.mode, kv == PDA_NVFP4); nw >= 2; --nw) {
     const size_t per_stage = static_cast<size_t>(nw) * (pl->stage_bytes + 8 + 4);
     const size_t meta = static_cast<size_t>(nw) * kMetaBytesPerWarp;
     if (fixed + meta >= static_cast<size_t>(kSmemBudget)) continue;
@@ -1017,8 +975,7 @@ using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnParams
 // The kernel for a unit of G_u query heads in the given mode.
 template <typename KV, typename QT, int D>
 KernelFn pick_g(int G_u, int mode) {
-  if constexpr (std::is_same<KV, fp8e4m3>::value || std::is_same<KV, nvfp4>::value ||
-                std::is_same<KV, __nv_bfloat16>::value) {
+  if constexpr (std::is_same<KV, fp8e4m3>::value || std::is_same<KV, nvfp4>::value) {
     if constexpr (D == 128) {
       if (mode == kModeTcPair) {
         switch (G_u) {
@@ -1086,18 +1043,15 @@ pda_status allow_max_smem(const void* fn, int dev) {
   return PDA_OK;
 }
 
-// Tensor-map shapes: rows as they are (3-D), a kv-head pair per box (4-D), and the bf16
-// split-row maps of encode_kv_split_tensor_map (K or V order, single or paired).
-enum MapKind { kMapRows, kMapPair, kMapSplitK, kMapSplitV, kMapSplitKPair, kMapSplitVPair };
-
 // The last few encoded KV tensor maps, keyed by everything the encoding depends on.
 struct MapKey {
   const void* base;
-  int num_blocks, block_size, H_kv, D, dtype, swizzle, kind;
+  int num_blocks, block_size, H_kv, D, dtype, swizzle;
+  bool pair;
   bool operator==(const MapKey& o) const {
     return base == o.base && num_blocks == o.num_blocks && block_size == o.block_size &&
            H_kv == o.H_kv && D == o.D && dtype == o.dtype && swizzle == o.swizzle &&
-           kind == o.kind;
+           pair == o.pair;
   }
 };
 constexpr int kMapCache = 8;
@@ -1106,12 +1060,12 @@ MapKey g_map_key[kMapCache];
 CUtensorMap g_map_val[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-// kMapPair: the two-head map of encode_kv_pair_tensor_map (byte caches; D = row bytes).
+// pair: the two-head map of encode_kv_pair_tensor_map (byte caches; D = row bytes).
 pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
                                 int block_size, int H_kv, int D, pda_dtype dtype,
-                                int swizzle_bytes, MapKind kind) {
+                                int swizzle_bytes, bool pair) {
   const MapKey key{base, num_blocks, block_size, H_kv, D, static_cast<int>(dtype),
-                   swizzle_bytes, static_cast<int>(kind)};
+                   swizzle_bytes, pair};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_map_used; ++i)
@@ -1120,22 +1074,10 @@ pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
         return PDA_OK;
       }
   }
-  pda_status st;
-  switch (kind) {
-    case kMapPair:
-      st = encode_kv_pair_tensor_map(tm, base, num_blocks, block_size, H_kv, D, swizzle_bytes);
-      break;
-    case kMapSplitK:
-    case kMapSplitV:
-    case kMapSplitKPair:
-    case kMapSplitVPair:
-      st = encode_kv_split_tensor_map(tm, base, num_blocks, block_size, H_kv, D,
-                                      kind == kMapSplitV || kind == kMapSplitVPair,
-                                      kind == kMapSplitKPair || kind == kMapSplitVPair);
-      break;
-    default:
-      st = encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype, swizzle_bytes);
-  }
+  const pda_status st =
+      pair ? encode_kv_pair_tensor_map(tm, base, num_blocks, block_size, H_kv, D, swizzle_bytes)
+           : encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype,
+                                  swizzle_bytes);
   if (st != PDA_OK) return st;
   std::lock_guard<std::mutex> lock(g_map_mu);
   g_map_key[g_map_next] = key;
@@ -1216,30 +1158,24 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   if (!make_plan(B, H_kv, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
   if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
 
-  const bool capped = is_capped(sm_cap, sms);
-  const Tiling tiling = tiling_for(kv_dtype, D, H_kv, G, capped);
+  const Tiling tiling = tiling_for(kv_dtype, D, H_kv, G);
   KernelFn fn = pick_kernel(kv_dtype, D, tiling);
   if (fn == nullptr) return PDA_ERR_UNSUPPORTED;
   st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
   if (st != PDA_OK) return st;
 
-  // the TMA sees an NVFP4 row as D/2 bytes; the quantised tensor-core steps read swizzled
-  // tiles whose swizzle span is one whole row (128 bytes FP8, 64 bytes NVFP4); bf16 rows
-  // (256 bytes) go through the split-row maps, K and V in their own orders
+  // the TMA sees an NVFP4 row as D/2 bytes; the tensor-core step reads swizzled tiles whose
+  // swizzle span is one whole row (128 bytes FP8, 64 bytes NVFP4)
   const int row_elems = kv_dtype == PDA_NVFP4 ? D / 2 : D;
   const pda_dtype map_type = kv_dtype == PDA_NVFP4 ? PDA_FP8_E4M3 : kv_dtype;
-  const bool tc = tiling.mode != kModeCuda;
+  const int swizzle = tiling.mode != kModeCuda ? row_elems : 0;
   const bool pair = tiling.mode == kModeTcPair;
-  const bool split = tc && kv_dtype == PDA_BF16;
-  const int swizzle = tc ? (split ? 128 : row_elems) : 0;
-  const MapKind kind_k = split ? (pair ? kMapSplitKPair : kMapSplitK) : pair ? kMapPair : kMapRows;
-  const MapKind kind_v = split ? (pair ? kMapSplitVPair : kMapSplitV) : pair ? kMapPair : kMapRows;
   CUtensorMap tmK, tmV;
   st = cached_kv_tensor_map(&tmK, k_cache, num_blocks, block_size, H_kv, row_elems, map_type,
-                            swizzle, kind_k);
+                            swizzle, pair);
   if (st != PDA_OK) return st;
   st = cached_kv_tensor_map(&tmV, v_cache, num_blocks, block_size, H_kv, row_elems, map_type,
-                            swizzle, kind_v);
+                            swizzle, pair);
   if (st != PDA_OK) return st;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);

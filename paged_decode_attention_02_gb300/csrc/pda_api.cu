@@ -2,7 +2,6 @@
 // TMA tensor-map encoder (obtained from the driver through the runtime, no -lcuda).
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -113,61 +112,6 @@ pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_
   const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base),
                               dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
-}
-
-pda_status encode_kv_split_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
-                                      int block_size, int H_kv, int D, bool v_order,
-                                      bool pair) {
-  std::call_once(g_encode_once, load_encoder);
-  if (g_encode == nullptr) return PDA_ERR_CUDA;
-  if ((D * 2) % 128 != 0 || (pair && H_kv % 2 != 0)) return PDA_ERR_INVALID_ARG;
-  const cuuint64_t line = 128;                             // bytes of one half
-  const cuuint64_t halves = static_cast<cuuint64_t>(D) * 2 / line;
-  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;    // bytes of one head's row
-  const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * block_size;
-  const cuuint64_t tok = static_cast<cuuint64_t>(H_kv) * row;  // bytes between tokens
-  const cuuint32_t bs = static_cast<cuuint32_t>(block_size);
-  const cuuint32_t nh = static_cast<cuuint32_t>(halves);
-  cuuint64_t dims[5];
-  cuuint64_t strides[4];
-  cuuint32_t box[5];
-  int rank;
-  if (!pair) {
-    rank = 4;
-    if (!v_order) {  // (d, half, head, row)
-      const cuuint64_t d[4] = {64, halves, static_cast<cuuint64_t>(H_kv), rows};
-      const cuuint64_t st[3] = {line, row, tok};
-      const cuuint32_t b[4] = {64, nh, 1, bs};
-      std::copy(d, d + 4, dims), std::copy(st, st + 3, strides), std::copy(b, b + 4, box);
-    } else {  // (d, row, half, head)
-      const cuuint64_t d[4] = {64, rows, halves, static_cast<cuuint64_t>(H_kv)};
-      const cuuint64_t st[3] = {tok, line, row};
-      const cuuint32_t b[4] = {64, bs, nh, 1};
-      std::copy(d, d + 4, dims), std::copy(st, st + 3, strides), std::copy(b, b + 4, box);
-    }
-  } else {
-    rank = 5;
-    const cuuint64_t np = static_cast<cuuint64_t>(H_kv / 2);
-    if (!v_order) {  // (d, half, row, head of the pair, pair)
-      const cuuint64_t d[5] = {64, halves, rows, 2, np};
-      const cuuint64_t st[4] = {line, tok, row, 2 * row};
-      const cuuint32_t b[5] = {64, nh, bs, 2, 1};
-      std::copy(d, d + 5, dims), std::copy(st, st + 4, strides), std::copy(b, b + 5, box);
-    } else {  // (d, row, half, head of the pair, pair)
-      const cuuint64_t d[5] = {64, rows, halves, 2, np};
-      const cuuint64_t st[4] = {tok, line, row, 2 * row};
-      const cuuint32_t b[5] = {64, bs, nh, 2, 1};
-      std::copy(d, d + 5, dims), std::copy(st, st + 4, strides), std::copy(b, b + 5, box);
-    }
-  }
-  const cuuint32_t elem_strides[5] = {1u, 1u, 1u, 1u, 1u};
-  // a head's row is 2 D >= 256 contiguous bytes, all of them used
-  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-                              const_cast<void*>(base), dims, strides, box, elem_strides,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PDA_OK : PDA_ERR_INVALID_ARG;
 }
 

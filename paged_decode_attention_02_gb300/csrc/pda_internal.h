@@ -30,17 +30,6 @@ pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_
                                      int block_size, int H_kv, int row_bytes,
                                      int swizzle_bytes);
 
-// Tiled tensor maps over a bf16 cache [num_blocks * block_size, H_kv, D] whose rows (2 D
-// bytes) are wider than the 128-byte swizzle span: each row is seen as 2 D / 128 halves of
-// 64 elements, every 128-byte half swizzled as one line. `v_order` false (the K side) puts
-// a tile in shared memory as [row][half]; true (the V side) as [half][row]. `pair` loads
-// the tiles of kv-heads 2h' and 2h' + 1 with one box, head 2h''s tile first (H_kv even).
-// Coordinates, innermost first: K (0, 0, head, row) or, paired, (0, 0, row, 0, pair);
-// V (0, row, 0, head) or (0, row, 0, 0, pair).
-pda_status encode_kv_split_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
-                                      int block_size, int H_kv, int D, bool v_order,
-                                      bool pair);
-
 inline size_t dtype_bytes(pda_dtype t) {
   return t == PDA_BF16 ? 2u : (t == PDA_FP8_E4M3 ? 1u : 4u);
 }

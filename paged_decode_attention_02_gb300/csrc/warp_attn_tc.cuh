@@ -1,5 +1,5 @@
-// warp_attn_tc.cuh -- one warp's tile step on the tensor cores at D = 128, for bf16 caches
-// and quantised ones (FP8 E4M3, and NVFP4: E2M1 codes with one E4M3 scale per 16 elements).
+// warp_attn_tc.cuh -- one warp's tile step on the tensor cores, for quantised caches
+// (FP8 E4M3, and NVFP4: E2M1 codes with one E4M3 scale per 16 elements) at D = 128.
 //
 // A head tile is one physical block (16 tokens) of one kv-head. Per head tile the warp
 // computes, with mma.sync m16n8k16 (fp16 operands, fp32 accumulators):
@@ -28,17 +28,11 @@
 // lo = fp16(p - hi), both multiplied into the same accumulator: one fp16 part alone
 // (relative error 2^-12) moves an output by up to 2^-12 of the largest |V|, which is too
 // much where the weighted V values cancel; the pair leaves about 2^-22.
-// bf16 caches need no conversion at all: q, K and V are bf16 operands as they are stored
-// (mma.sync with bf16 inputs), and the probabilities are split into two bf16 parts
-// (together about 2^-17 relative).
 //
 // Shared-memory layout: the TMA writes each 16-row head tile with the 128-byte swizzle (FP8,
 // 128-byte rows: 16-byte chunk c of row r lands at chunk c ^ (r & 7)) or the 64-byte
 // swizzle (NVFP4, 64-byte rows: chunk c ^ ((r >> 1) & 3)), which makes every load below
-// free of bank conflicts. A bf16 row is 256 bytes, two 128-byte halves, each swizzled as a
-// 128-byte line L (chunk c at c ^ (L & 7)): K tiles hold line L = 2 r + half, V tiles
-// L = 16 half + r (the two K and V tensor maps order their boxes differently), the orders
-// under which the K fragment loads and the V ldmatrix rows are both conflict-free. The element order along d inside a k-step is permuted (the same
+// free of bank conflicts. The element order along d inside a k-step is permuted (the same
 // permutation for q and K), which leaves the dot products unchanged.
 #pragma once
 
@@ -54,34 +48,13 @@ template <typename KV, int D>
 struct TCOps {
   static_assert(D == 128, "tensor-core tile step is laid out for D = 128");
   static constexpr bool FP4 = std::is_same<KV, nvfp4>::value;
-  static constexpr bool BF = std::is_same<KV, __nv_bfloat16>::value;
-  static_assert(FP4 || BF || std::is_same<KV, fp8e4m3>::value, "bf16, FP8 or NVFP4 caches");
-  static constexpr int ROW_BYTES = FP4 ? D / 2 : (BF ? 2 * D : D);  // one K or V row
+  static_assert(FP4 || std::is_same<KV, fp8e4m3>::value, "quantised caches only");
+  static constexpr int ROW_BYTES = FP4 ? D / 2 : D;  // bytes of one K or V row
   static constexpr int TILE_BYTES = 16 * ROW_BYTES;  // one head tile
-  static constexpr int HALF_TILE = 16 * 128;  // bf16 V: the 16 rows of one 128-byte half
-  // d of the second output row a lane holds for m-tile i (row g + 8): d_of + this
-  static constexpr int ROW2_STEP = BF ? 8 : 1;
-
-  static __device__ __forceinline__ void mma(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                             uint32_t a3, uint32_t b0, uint32_t b1) {
-    if constexpr (BF)
-      mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
-    else
-      mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
-  }
 
   // ldmatrix row addresses of this lane inside a V head tile (bytes), one per pair of
   // 16-byte chunks.
   static __device__ __forceinline__ void v_offsets(int lane, int* v_off) {
-    if constexpr (BF) {
-      // m-tile i reads chunks 2i (matrices 0, 2) and 2i + 1 (1, 3) of tokens 0-7 (0, 1) and
-      // 8-15 (2, 3); entry q serves m-tiles q and q + 4 (+ HALF_TILE)
-      const int tok = (lane & 7) + 8 * (lane >> 4);
-      const int ch = (lane >> 3) & 1;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v_off[q] = tok * 128 + (((2 * q + ch) ^ (tok & 7)) << 4);
-      return;
-    }
     const int j = lane & 7;                   // row inside the 8x8 matrix this lane addresses
     const int r = j + 8 * ((lane >> 3) & 1);  // token row of the tile
     const int ch = lane >> 4;                 // second chunk of the pair
@@ -104,22 +77,6 @@ struct TCOps {
     }
   }
 
-  // bf16: q of row `row` (d 32 t4 .. 32 t4 + 31) as A fragments in the same k-step order as
-  // q_fragments, straight from shared memory; zeros if `real` is false.
-  static __device__ __forceinline__ void q_fragments_bf16(const __nv_bfloat16* q_smem, int row,
-                                                          bool real, int t4,
-                                                          uint32_t (&qa)[8][2]) {
-    const uint4* src = reinterpret_cast<const uint4*>(q_smem + row * D + 32 * t4);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 w = real ? src[i] : make_uint4(0u, 0u, 0u, 0u);
-      qa[2 * i][0] = w.x;
-      qa[2 * i][1] = w.y;
-      qa[2 * i + 1][0] = w.z;
-      qa[2 * i + 1][1] = w.w;
-    }
-  }
-
   // S[nt] += Q K^T over one head tile: n-tile nt covers tokens 8 nt .. 8 nt + 7 (token g of
   // it on this lane). ksc: the tile's block scales, row r at ksc + r * ksc_stride (NVFP4).
   static __device__ __forceinline__ void qk(float (&sc)[2][4], const uint32_t (&qa)[8][2],
@@ -128,19 +85,7 @@ struct TCOps {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int r = g + 8 * nt;
-      if constexpr (BF) {
-        // logical chunk 4 t4 + i = d 32 t4 + 8 i .. + 7: k-steps 2 i (words x, y) and
-        // 2 i + 1 (z, w), already the B fragments
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 4 * t4 + i;
-          const int L = 2 * r + (c >> 3);
-          const uint4 w =
-              *reinterpret_cast<const uint4*>(ks + L * 128 + (((c & 7) ^ (L & 7)) << 4));
-          mma(sc[nt], qa[2 * i][0], 0u, qa[2 * i][1], 0u, w.x, w.y);
-          mma(sc[nt], qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, w.z, w.w);
-        }
-      } else if constexpr (FP4) {
+      if constexpr (FP4) {
         // 16 bytes = d 32 t4 .. 32 t4 + 31; byte 2s (+1) holds k-step s's first (second) pair
         const uint4 w = *reinterpret_cast<const uint4*>(
             ks + r * ROW_BYTES + ((t4 ^ ((r >> 1) & 3)) << 4));
@@ -186,7 +131,7 @@ struct TCOps {
                                                     uint32_t& keep_hi) {
     const bool a = 2 * t4 < n_valid, b = 2 * t4 + 1 < n_valid;
     const bool c = 8 + 2 * t4 < n_valid, d = 9 + 2 * t4 < n_valid;
-    if constexpr (FP4 || BF) {
+    if constexpr (FP4) {
       keep_lo = (a ? 0x0000ffffu : 0u) | (b ? 0xffff0000u : 0u);
       keep_hi = (c ? 0x0000ffffu : 0u) | (d ? 0xffff0000u : 0u);
     } else {
@@ -204,19 +149,7 @@ struct TCOps {
                                             const int (&v_off)[4], int g, int t4,
                                             uint32_t pb0, uint32_t pb1, uint32_t pl0,
                                             uint32_t pl1, uint32_t keep_lo, uint32_t keep_hi) {
-    if constexpr (BF) {
-      // ldmatrix.trans of m-tile i (d 16 i .. 16 i + 15) gives the A fragment directly:
-      // word 0 = (d 16 i + g; tokens 2t4, 2t4 + 1), 1 = (d + 8; same), 2, 3 = tokens + 8
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t r[4];
-        ldmatrix_x4_trans(r, vs + v_off[i & 3] + (i >> 2) * HALF_TILE);
-        const uint32_t a0 = r[0] & keep_lo, a1 = r[1] & keep_lo;
-        const uint32_t a2 = r[2] & keep_hi, a3 = r[3] & keep_hi;
-        mma(o[i], a0, a1, a2, a3, pb0, pb1);
-        mma(o[i], a0, a1, a2, a3, pl0, pl1);
-      }
-    } else if constexpr (FP4) {
+    if constexpr (FP4) {
       // scale pairs (token t0, token t0 + 1) of this lane's block in chunk c: rows 2t4(+1)
       // and 8 + 2t4 (+1); the block is 2c + g / 4
       const uint2 w0 = *reinterpret_cast<const uint2*>(vsc + (2 * t4) * vsc_stride);
@@ -286,7 +219,7 @@ struct TCOps {
 
   // d of row g of m-tile i (row g + 8 is d + 1).
   static __device__ __forceinline__ int d_of(int i, int g) {
-    return BF ? 16 * i + g : FP4 ? 32 * (i >> 1) + 4 * g + 2 * (i & 1) : 16 * i + 2 * g;
+    return FP4 ? 32 * (i >> 1) + 4 * g + 2 * (i & 1) : 16 * i + 2 * g;
   }
 
   // Power-of-two factor that brings max |q| (over the warp) below 2^15: returns `down`, the
@@ -329,17 +262,9 @@ struct TCOps {
     return amax;
   }
 
-  // fp16 (bf16 for bf16 caches) hi and lo parts of two probabilities as x2 words.
+  // fp16 hi and lo parts of two probabilities as f16x2 words.
   static __device__ __forceinline__ void split_p(float p0, float p1, uint32_t& hi,
                                                  uint32_t& lo) {
-    if constexpr (BF) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-      const float2 r = __bfloat1622float2(h);
-      const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - r.x, p1 - r.y);
-      hi = *reinterpret_cast<const uint32_t*>(&h);
-      lo = *reinterpret_cast<const uint32_t*>(&l);
-      return;
-    }
     const __half2 h = __floats2half2_rn(p0, p1);
     const float2 r = __half22float2(h);
     hi = f16x2_bits(h);
@@ -396,17 +321,12 @@ struct WarpAttnTC {
 
   // q of this warp's segment (G rows of D bf16 in shared memory), pre-scale scale_log2.
   __device__ __forceinline__ void reset(const __nv_bfloat16* q_smem, float scale_log2) {
-    if constexpr (Ops::BF) {
-      Ops::q_fragments_bf16(q_smem, g, g < G, t4, qa);
-      c = scale_log2;
-    } else {
-      float qv[32];
-      const float amax = Ops::load_q(q_smem, g, g < G, t4, qv);
-      float up;
-      const float down = Ops::q_shift(amax, up);
-      c = scale_log2 * up;
-      Ops::q_fragments(qv, down, qa);
-    }
+    float qv[32];
+    const float amax = Ops::load_q(q_smem, g, g < G, t4, qv);
+    float up;
+    const float down = Ops::q_shift(amax, up);
+    c = scale_log2 * up;
+    Ops::q_fragments(qv, down, qa);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -477,13 +397,8 @@ struct WarpAttnTC {
       for (int jj = 0; jj < 2; ++jj) {
         const int j = 2 * t4 + jj;
         if (j < G) {
-          if constexpr (Ops::ROW2_STEP == 1) {
-            const float v[2] = {o[i][jj], o[i][2 + jj]};
-            f(j, Ops::d_of(i, g), v, 2, l_cols[jj]);
-          } else {  // rows g and g + 8 hold d and d + 8
-            f(j, Ops::d_of(i, g), &o[i][jj], 1, l_cols[jj]);
-            f(j, Ops::d_of(i, g) + Ops::ROW2_STEP, &o[i][2 + jj], 1, l_cols[jj]);
-          }
+          const float v[2] = {o[i][jj], o[i][2 + jj]};
+          f(j, Ops::d_of(i, g), v, 2, l_cols[jj]);
         }
       }
     }
@@ -521,20 +436,14 @@ struct WarpAttnTCPair {
   }
 
   __device__ __forceinline__ void reset(const __nv_bfloat16* q_smem, float scale_log2) {
-    if constexpr (Ops::BF) {
-      Ops::q_fragments_bf16(q_smem, g, g < GH, t4, qa[0]);
-      Ops::q_fragments_bf16(q_smem, GH + g, g < GH, t4, qa[1]);
-      c = scale_log2;
-    } else {
-      float qa_v[32], qb_v[32];
-      const float amax = fmaxf(Ops::load_q(q_smem, g, g < GH, t4, qa_v),
-                               Ops::load_q(q_smem, GH + g, g < GH, t4, qb_v));
-      float up;
-      const float down = Ops::q_shift(amax, up);
-      c = scale_log2 * up;
-      Ops::q_fragments(qa_v, down, qa[0]);
-      Ops::q_fragments(qb_v, down, qa[1]);
-    }
+    float qa_v[32], qb_v[32];
+    const float amax = fmaxf(Ops::load_q(q_smem, g, g < GH, t4, qa_v),
+                             Ops::load_q(q_smem, GH + g, g < GH, t4, qb_v));
+    float up;
+    const float down = Ops::q_shift(amax, up);
+    c = scale_log2 * up;
+    Ops::q_fragments(qa_v, down, qa[0]);
+    Ops::q_fragments(qb_v, down, qa[1]);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -650,13 +559,8 @@ struct WarpAttnTCPair {
         const int local = n & 3;                 // head within its kv-head
         const int j = n < 4 ? local : GH + local;  // unit head
         if (local < GH) {
-          if constexpr (Ops::ROW2_STEP == 1) {
-            const float v[2] = {o[i][jj], o[i][2 + jj]};
-            f(j, Ops::d_of(i, g), v, 2, l_cols[jj]);
-          } else {  // rows g and g + 8 hold d and d + 8
-            f(j, Ops::d_of(i, g), &o[i][jj], 1, l_cols[jj]);
-            f(j, Ops::d_of(i, g) + Ops::ROW2_STEP, &o[i][2 + jj], 1, l_cols[jj]);
-          }
+          const float v[2] = {o[i][jj], o[i][2 + jj]};
+          f(j, Ops::d_of(i, g), v, 2, l_cols[jj]);
         }
       }
     }

@@ -115,7 +115,7 @@ def test_full_size_pack_of_longest_requests():
 
 
 # ------------------------------------------------------------------ shapes and dtypes
-SHAPES = [  # (dtype, D, H, H_kv); bf16 at D = 128 runs on the tensor cores except G = 1, odd H_kv
+SHAPES = [  # (dtype, D, H, H_kv)
     ("bf16", 128, 32, 32), ("bf16", 128, 32, 16), ("bf16", 128, 32, 8), ("bf16", 128, 32, 4),
     ("bf16", 128, 12, 3), ("bf16", 128, 7, 7), ("bf16", 128, 16, 2),
     ("bf16", 64, 16, 16), ("bf16", 64, 16, 8), ("bf16", 64, 16, 4), ("bf16", 64, 16, 2),
@@ -630,10 +630,10 @@ def test_nvfp4_scale_calls_edge_cases():
 
 
 # ------------------------------------------------------------------ tensor-core tile step
-# At D = 128, FP8 and NVFP4 caches run their dot products on the tensor cores with fp16
-# operands (q brought into fp16 range by a power-of-two shift), bf16 caches with bf16
-# operands; in both a head's running maximum may lag the true one by up to 2^8 before the
-# output is rescaled. G = 1 with odd H_kv takes the CUDA-core path.
+# FP8 and NVFP4 caches at D = 128 with G >= 2 run their dot products on the tensor cores
+# with fp16 operands: q is brought into fp16 range by a power-of-two shift, and a head's
+# running maximum may lag the true one by up to 2^8 before the output is rescaled. The
+# G = 1 workloads below take the CUDA-core path and check the same edge cases there.
 QUANTISED = ["gqa_skew_b256_fp8", "llama2_13b_b80_fp8", "gqa_skew_b256_nvfp4",
              "llama2_13b_b80_nvfp4"]
 
@@ -653,7 +653,7 @@ def test_tc_q_far_outside_fp16_range(name):
     assert_attention_close(out, ref, f"{name} q x 2^20")
 
 
-@pytest.mark.parametrize("name", QUANTISED + ["gqa_skew_b256", "llama2_13b_b80"])
+@pytest.mark.parametrize("name", QUANTISED)
 @pytest.mark.parametrize("boost", [8.0, 40.0])
 def test_tc_sharp_softmax_rescales(name, boost):
     """A scale `boost` times larger spreads the scores over tens of log2 units, so later
@@ -671,9 +671,10 @@ def test_tc_sharp_softmax_rescales(name, boost):
 @pytest.mark.parametrize("kv", ["fp8", "nvfp4", "bf16"])
 @pytest.mark.parametrize("H,H_kv", [(64, 8), (16, 8), (8, 8), (12, 3), (7, 7)])
 def test_tc_groups_with_ragged_tails(kv, H, H_kv):
-    """Group sizes 8 and 2 (tensor cores) and 1 (CUDA cores), lengths that end at every
-    offset of a block (partial tiles mask tokens 1..15 of the last block; the unused rows
-    hold NaN, or NaN block scales, so an unmasked one would show)."""
+    """Group sizes 8 and 2 (tensor cores for quantised caches) and 1, lengths that end at
+    every offset of a block (partial tiles mask tokens 1..15 of the last block; the unused
+    rows hold NaN, or NaN block scales, so an unmasked one would show). bf16 runs the same
+    cases on the CUDA cores."""
     base = {"fp8": "gqa_skew_b256_fp8", "nvfp4": "gqa_skew_b256_nvfp4",
             "bf16": "gqa_skew_b256"}[kv]
     lens = np.array(list(range(1, 17)) + [47, 64, 65, 333], np.int32)
