@@ -152,8 +152,10 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  *                 the library gives each call. (A call captured in a CUDA graph keeps its
  *                 number on every replay; if a replay ever reports PDA_DEVERR_TIMEOUT, zero
  *                 the workspace before the next replay.)
- *  Supported: D in {64, 128}, block_size == 16, H / H_kv in {1, 2, 4, 8}, B <= 8192,
- *  kv_dtype in {PDA_F32, PDA_BF16}. Pointers 16-byte aligned.
+ *  Supported: D in {64, 128}; block_size in {16, 32, 64, 128, 256} (the kernel works in
+ *  tiles of 16 rows of one physical block); H / H_kv in {1, 2, 4, 8}; B <= 8192;
+ *  kv_dtype in {PDA_F32, PDA_BF16}. Pointers 16-byte aligned. Other sizes return
+ *  PDA_ERR_UNSUPPORTED.
  */
 pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                       const void* v_cache, const int32_t* block_tables,
@@ -212,10 +214,10 @@ pda_status pda_paged_decode_attention_fp8(void* out, const void* q, const void* 
  *
  *  k_data, v_data   [num_blocks, block_size, H_kv, D / 2] bytes.
  *  k_block_scales, v_block_scales [num_blocks, H_kv, block_size, D / 16] E4M3 bytes,
- *                   16-byte aligned: per block and head-major, so the scales of one
- *                   (block, kv-head) tile are one contiguous run of block_size * D / 16
+ *                   16-byte aligned: per block and head-major, so the scales of the 16
+ *                   rows of one kv-head that a tile covers are one contiguous run of D
  *                   bytes (the pages give no layout; this is the one the kernel reads in
- *                   one bulk copy per tile).
+ *                   one bulk copy per tile and head).
  *  q                [B, H, D] in q_dtype, which must be PDA_BF16.
  *  k_scale, v_scale finite per-tensor scales.
  *  Every other argument, the workspace (pda_attention_workspace_size with PDA_NVFP4), the

@@ -112,6 +112,8 @@ struct AttnParams {
   const uint8_t* k_bscales;       // NVFP4: [blocks, H_kv, 16, D/16] E4M3 block scales
   const uint8_t* v_bscales;
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
+  int block_size;                 // tokens per physical block: 16 << bs_shift
+  int bs_shift;                   // log2 of the 16-row tiles per physical block
   int out_bf16;
   float scale_log2;
   int num_workers;
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
       (reinterpret_cast<uintptr_t>(s_info + nwarps * p.stages) + 7) & ~uintptr_t(7));
 
   // ---- 1. block prefix sums of per-request tile counts (every block computes its own)
-  const int cap_tokens = min(p.max_blocks * kBS, p.max_context_len);
+  const int cap_tokens = min(p.max_blocks * p.block_size, p.max_context_len);
   {
     const int per = (B + blockDim.x - 1) / blockDim.x;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
@@ -714,8 +716,9 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
     if (y < t_end) {
       int nb;
       locate(y, nxt_b, nxt_h, nxt_blk, nb);
-      cp_async4(&my_meta[buf * 32 + lane].x,
-                p.block_tables + static_cast<size_t>(nxt_b) * p.max_blocks + nxt_blk);
+      cp_async4(&my_meta[buf * 32 + lane].x, p.block_tables +
+                                                     static_cast<size_t>(nxt_b) * p.max_blocks +
+                                                     (nxt_blk >> p.bs_shift));
       cp_async4(&my_meta[buf * 32 + lane].y, p.context_lens + nxt_b);
     }
     cp_async_commit();
@@ -744,12 +747,28 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
       if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
       const uint32_t bytes = 2 * kTile + 2 * kScales + (need_q ? Geo::Q_BYTES : 0);
       mbar_arrive_expect_tx(&my_bar[s], bytes);
-      const int row = (bad ? 0 : cur_pid) * kBS;
+      // the tile is rows sub * 16 .. + 15 of its physical block
+      const int sub = cur_blk & ((1 << p.bs_shift) - 1);
+      const int row = (bad ? 0 : cur_pid) * p.block_size + sub * kBS;
       if constexpr (Geo::SCALED) {
-        // the unit's scales are one run per block: [kHeads][16][D/16] at unit cur_h
-        const size_t off = (static_cast<size_t>(bad ? 0 : cur_pid) * H_kv + cur_h) * kScales;
-        bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
-        bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
+        // scales [blocks][heads][block_size][D/16]: each head's 16 rows are one run; with
+        // 16-token blocks a pair's two runs are adjacent (one copy)
+        constexpr uint32_t kRun = Geo::SCALE_BYTES;  // one head's 16 rows
+        const size_t head0 = static_cast<size_t>(bad ? 0 : cur_pid) * H_kv * kHeads +
+                             static_cast<size_t>(cur_h) * kHeads;
+        const size_t off = (head0 * p.block_size + static_cast<size_t>(sub) * kBS) *
+                           Geo::ROW_SCALES;
+        if (kHeads == 1 || p.bs_shift == 0) {
+          bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
+          bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
+        } else {
+          const size_t step = static_cast<size_t>(p.block_size) * Geo::ROW_SCALES;
+#pragma unroll
+          for (int u = 0; u < kHeads; ++u) {
+            bulk_load(ks_buf(s) + u * kRun, p.k_bscales + off + u * step, kRun, &my_bar[s]);
+            bulk_load(vs_buf(s) + u * kRun, p.v_bscales + off + u * step, kRun, &my_bar[s]);
+          }
+        }
       }
       if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
         tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
@@ -1023,6 +1042,10 @@ KernelFn pick_kernel(pda_dtype kv, int D, const Tiling& t) {
 }
 
 bool supported_g(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+// Physical blocks of 16, 32, ..., 256 tokens (a tile is 16 rows of one block).
+bool supported_block_size(int bs) {
+  return bs >= kBS && bs <= 16 * kBS && (bs & (bs - 1)) == 0;
+}
 
 // Numbers the calls, so a call recognises arrival counters left by earlier ones.
 std::atomic<unsigned long long> g_call{1};
@@ -1074,10 +1097,12 @@ pda_status cached_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
         return PDA_OK;
       }
   }
+  // boxes are one tile: kBS rows of one physical block (block_size is a multiple of kBS)
   const pda_status st =
-      pair ? encode_kv_pair_tensor_map(tm, base, num_blocks, block_size, H_kv, D, swizzle_bytes)
+      pair ? encode_kv_pair_tensor_map(tm, base, num_blocks, block_size, H_kv, D, swizzle_bytes,
+                                       kBS)
            : encode_kv_tensor_map(tm, base, num_blocks, block_size, H_kv, D, dtype,
-                                  swizzle_bytes);
+                                  swizzle_bytes, kBS);
   if (st != PDA_OK) return st;
   std::lock_guard<std::mutex> lock(g_map_mu);
   g_map_key[g_map_next] = key;
@@ -1098,7 +1123,8 @@ extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D
   if (bytes == nullptr || B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 ||
       block_size <= 0 || sm_cap < 0 || !(dtype_ok(kv_dtype) || kv_dtype == PDA_NVFP4))
     return PDA_ERR_INVALID_ARG;
-  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(H / H_kv) || B > kMaxBatch)
+  if (!supported_block_size(block_size) || (D != 64 && D != 128) || !supported_g(H / H_kv) ||
+      B > kMaxBatch)
     return PDA_ERR_UNSUPPORTED;
   int dev, sms;
   const pda_status st = current_device_sms(&dev, &sms);
@@ -1142,7 +1168,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   const int G = H / H_kv;
   const bool quantised = kv_dtype == PDA_FP8_E4M3 || kv_dtype == PDA_NVFP4;
   const bool q_ok = quantised ? q_dtype == PDA_BF16 : q_dtype == kv_dtype;
-  if (block_size != kBS || (D != 64 && D != 128) || !supported_g(G) || !q_ok ||
+  if (!supported_block_size(block_size) || (D != 64 && D != 128) || !supported_g(G) || !q_ok ||
       B > kMaxBatch)
     return PDA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31) ||
@@ -1198,6 +1224,9 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.num_blocks = num_blocks;
   ap.max_blocks = max_blocks_per_seq;
   ap.max_context_len = max_context_len;
+  ap.block_size = block_size;
+  ap.bs_shift = 0;
+  while ((kBS << ap.bs_shift) < block_size) ++ap.bs_shift;
   ap.out_bf16 = out_dtype == PDA_BF16;
   // the K scale folds into q's pre-scale: s = scale * (k_scale * code) . q
   ap.scale_log2 = scale * k_scale * 1.4426950408889634f;

@@ -48,9 +48,10 @@ pda_status current_device_sms(int* device, int* num_sms) {
 
 pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
                                 int block_size, int H_kv, int D, pda_dtype dtype,
-                                int swizzle_bytes) {
+                                int swizzle_bytes, int box_rows) {
   if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128)
     return PDA_ERR_INVALID_ARG;
+  if (box_rows <= 0 || box_rows > 256 || block_size % box_rows != 0) return PDA_ERR_INVALID_ARG;
   std::call_once(g_encode_once, load_encoder);
   if (g_encode == nullptr) return PDA_ERR_CUDA;
   const cuuint64_t e = dtype_bytes(dtype);
@@ -58,7 +59,7 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
                               static_cast<cuuint64_t>(num_blocks) * block_size};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e,
                                  static_cast<cuuint64_t>(H_kv) * D * e};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(block_size)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   const CUtensorMapDataType dt = dtype == PDA_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                  : dtype == PDA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -87,9 +88,10 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
 
 pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_blocks,
                                      int block_size, int H_kv, int row_bytes,
-                                     int swizzle_bytes) {
+                                     int swizzle_bytes, int box_rows) {
   std::call_once(g_encode_once, load_encoder);
   if (g_encode == nullptr) return PDA_ERR_CUDA;
+  if (box_rows <= 0 || box_rows > 256 || block_size % box_rows != 0) return PDA_ERR_INVALID_ARG;
   if (H_kv % 2 != 0 || (swizzle_bytes != 0 && swizzle_bytes != row_bytes) ||
       (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128))
     return PDA_ERR_INVALID_ARG;
@@ -98,7 +100,7 @@ pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_
   const cuuint64_t dims[4] = {X, static_cast<cuuint64_t>(num_blocks) * block_size, 2,
                               static_cast<cuuint64_t>(H_kv / 2)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H_kv) * X, X, 2 * X};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(X), static_cast<cuuint32_t>(block_size),
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(X), static_cast<cuuint32_t>(box_rows),
                              2u, 1u};
   const cuuint32_t elem_strides[4] = {1u, 1u, 1u, 1u};
   const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B

@@ -64,7 +64,10 @@ def _attn(lib, **kw):
     (dict(scale=float("nan")), binding.PDA_ERR_INVALID_ARG),
     (dict(out=ctypes.c_void_p((1 << 20) + 4)), binding.PDA_ERR_INVALID_ARG),  # misaligned
     (dict(D=96), binding.PDA_ERR_UNSUPPORTED),
-    (dict(bs=32), binding.PDA_ERR_UNSUPPORTED),
+    (dict(bs=24), binding.PDA_ERR_UNSUPPORTED),          # not a multiple of the 16-row tile
+    (dict(bs=8), binding.PDA_ERR_UNSUPPORTED),
+    (dict(bs=48), binding.PDA_ERR_UNSUPPORTED),          # not a power of two
+    (dict(bs=512), binding.PDA_ERR_UNSUPPORTED),
     (dict(H=24, H_kv=2), binding.PDA_ERR_UNSUPPORTED),   # group of 12
     (dict(qd=0), binding.PDA_ERR_UNSUPPORTED),           # q dtype != kv dtype
     (dict(B=9000), binding.PDA_ERR_UNSUPPORTED),

@@ -731,3 +731,71 @@ def test_quantised_single_very_long_request_split_over_every_worker(name):
     out, err = gpu_step(s, append=False)
     assert err == 0
     assert_attention_close(out, ref, f"{name} one long request")
+
+
+# ------------------------------------------------------------------ physical block sizes
+# Blocks of 32, 64, 128 or 256 tokens: the attention works in 16-row tiles of one block, a
+# block holding block_size / 16 of them; append and pack move whole rows whatever the size.
+BLOCK_SIZE_CASES = [("gqa_skew_b256", {}), ("llama2_13b_b80", {}),
+                    ("llama2_13b_b80", {"D": 64, "H": 16, "H_kv": 4}),
+                    ("tiny", {}),
+                    ("gqa_skew_b256_fp8", {}), ("gqa_skew_b256_nvfp4", {}),
+                    ("llama2_13b_b80_nvfp4", {}), ("gqa_skew_b256_nvfp4", {"H": 12, "H_kv": 3})]
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128, 256])
+@pytest.mark.parametrize("name,kw", BLOCK_SIZE_CASES)
+def test_block_sizes_full_step(name, kw, bs):
+    """Append then attention with lengths ending at every kind of offset: inside the first
+    tile of a block, at tile and block boundaries, one past them; unused rows poisoned."""
+    lens = np.array([1, 15, 16, 17, 31, 32, 33, bs - 1, bs, bs + 1, 3 * bs + 5, 700], np.int32)
+    w = variant(name, block_size=bs, B=len(lens), lengths="uniform:1,700", **kw)
+    s = wl.make_step(w, device=DEV, lengths=lens, poison_unused=True)
+    ksc = vsc = None
+    if s.w.kv == "nvfp4":
+        ksc, vsc = to_np(s.k_bscales).copy(), to_np(s.v_bscales).copy()
+        assert orc.kv_append_block_scales(to_np(s.k_new_bscales), to_np(s.v_new_bscales), ksc,
+                                          vsc, s.slot_mapping_np) == 0
+    ref, st, kc, vc = oracle_full_step(s)
+    assert st == 0 and np.isfinite(ref).all()
+    out, err = gpu_step(s)
+    assert err == 0
+    # bitwise (the poisoned rows hold NaN, which compares unequal as a float)
+    assert np.array_equal(to_np(s.k_cache).view(np.uint8), kc.view(np.uint8))
+    assert np.array_equal(to_np(s.v_cache).view(np.uint8), vc.view(np.uint8))
+    if ksc is not None:
+        assert np.array_equal(to_np(s.k_bscales), ksc) and np.array_equal(to_np(s.v_bscales), vsc)
+    assert_attention_close(out, ref, f"{name} {kw} block_size={bs}")
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+def test_block_sizes_pack_unpack_and_caps(bs):
+    """Pack and unpack of whole requests, and SM-capped attention, over 32- and 64-token
+    blocks."""
+    s = wl.make_step(variant("gqa_skew_b256", block_size=bs, B=12), device=DEV)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0
+    for cap in (3, 61, 0):
+        out, err = gpu_step(s, append=False, sm_cap=cap)
+        assert err == 0
+        assert_attention_close(out, ref, f"block_size={bs} sm_cap={cap}")
+    kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
+    r = int(np.argmax(s.context_lens_np))
+    L = int(s.context_lens_np[r])
+    packed = torch.empty((L, 2, s.w.H_kv, s.w.D), dtype=s.k_cache.dtype, device=DEV)
+    pda.kv_pack_blocks(packed, s.k_cache, s.v_cache, s.block_tables[r], L)
+    want, st = orc.kv_pack_blocks(kc, vc, s.block_tables_np[r], L)
+    assert st == 0 and np.array_equal(to_np(packed), want)
+    k2, v2 = torch.zeros_like(s.k_cache), torch.zeros_like(s.v_cache)
+    pda.kv_unpack_blocks(packed, k2, v2, s.block_tables[r], L)
+    kw, vw = np.zeros_like(kc), np.zeros_like(vc)
+    assert orc.kv_unpack_blocks(want, kw, vw, s.block_tables_np[r], L) == 0
+    assert np.array_equal(to_np(k2), kw) and np.array_equal(to_np(v2), vw)
+
+
+@pytest.mark.parametrize("bs", [8, 24, 48, 512])
+def test_unsupported_block_sizes_are_rejected(bs):
+    s = wl.make_step(variant("gqa_skew_b256", block_size=bs, B=2), device=DEV)
+    with pytest.raises(binding.PdaError) as e:
+        pda.alloc_workspace(s.B, s.w.H, s.w.H_kv, s.w.D, bs, s.w.torch_dtype, device=DEV)
+    assert e.value.status == binding.PDA_ERR_UNSUPPORTED
