@@ -26,7 +26,7 @@
  *      s_t = scale * sum_d q[d] * K_t[d]            for t < L
  *      p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
  *      out = sum_t p_t * V_t
- * Everything is computed in double; stored bf16/fp32 inputs are upcast exactly, and FP8
+ * Everything is computed in double; stored bf16/fp16/fp32 inputs are upcast exactly, and FP8
  * E4M3 codes are decoded exactly and multiplied by their tensor's scale. Quantised KV
  * caches (page "From PagedAttention to Prefill-Decode disaggregation", sec. 6.2: a 4-bit KV
  * cache dequantised to FP8 before attention) are read through that decode.
@@ -52,16 +52,35 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8_E4M3 = 2, ORC_NVFP4 = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8_E4M3 = 2, ORC_NVFP4 = 3, ORC_F16 = 4 };
 enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_DATA = 4 };
 
 static size_t orc_elem_size(int dtype) {
-  return dtype == ORC_BF16 ? 2u : (dtype == ORC_FP8_E4M3 ? 1u : 4u);
+  return (dtype == ORC_BF16 || dtype == ORC_F16) ? 2u : (dtype == ORC_FP8_E4M3 ? 1u : 4u);
 }
 
 static int orc_dtype_ok(int dtype) {
-  return dtype == ORC_F32 || dtype == ORC_BF16 || dtype == ORC_FP8_E4M3;
+  return dtype == ORC_F32 || dtype == ORC_BF16 || dtype == ORC_FP8_E4M3 || dtype == ORC_F16;
 }
+
+/*
+ * IEEE 754 binary16: sign bit, 5 exponent bits with bias 15, 10 mantissa bits. Exponent 0
+ * encodes the subnormals m * 2^-24; exponent 31 is infinity (m = 0) or NaN; every other
+ * code is (1 + m/1024) * 2^(e - 15) = (1024 + m) * 2^(e - 25).
+ */
+static double orc_f16(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+  double mag;
+  if (e == 31)
+    mag = m ? NAN : INFINITY;
+  else if (e == 0)
+    mag = ldexp((double)m, -24);
+  else
+    mag = ldexp((double)(1024 + m), e - 25);
+  return sign ? -mag : mag;
+}
+
+double oracle_decode_f16(int bits) { return orc_f16((uint16_t)(bits & 0xffff)); }
 
 /*
  * FP8 E4M3 (the OCP 8-bit format with no infinities): sign bit, 4 exponent bits with bias
@@ -93,6 +112,11 @@ double oracle_decode_e2m1(int code) { return orc_e2m1((unsigned)(code & 15)); }
 /* Exact upcast of stored element idx. A bf16 value is the upper 16 bits of a binary32. */
 static double orc_load(const void* base, size_t idx, int dtype) {
   if (dtype == ORC_FP8_E4M3) return orc_e4m3(((const uint8_t*)base)[idx]);
+  if (dtype == ORC_F16) {
+    uint16_t h;
+    memcpy(&h, (const char*)base + idx * 2u, 2u);
+    return orc_f16(h);
+  }
   if (dtype == ORC_BF16) {
     uint16_t h;
     memcpy(&h, (const char*)base + idx * 2u, 2u);

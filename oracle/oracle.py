@@ -5,7 +5,7 @@ of ``bench.py`` use this module. It imports nothing from the CUDA library and th
 library imports nothing from it.
 
 Arrays are NumPy arrays. A bf16 tensor is passed as its raw bits in a ``uint16`` array;
-an fp32 tensor as ``float32``. What each function computes, and the page sections it
+an fp16 tensor as ``float16``; an fp32 tensor as ``float32``. What each function computes, and the page sections it
 follows, is stated in ``oracle.c``.
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-ORC_F32, ORC_BF16, ORC_FP8_E4M3 = 0, 1, 2
+ORC_F32, ORC_BF16, ORC_FP8_E4M3, ORC_F16 = 0, 1, 2, 4
 ORC_OK, ORC_ERR_ARG, ORC_ERR_DATA = 0, 1, 4
 
 _lock = threading.Lock()
@@ -61,6 +61,8 @@ def load(path: str | None = None):
         lib.oracle_decode_e4m3.restype = ctypes.c_double
         lib.oracle_decode_e2m1.argtypes = [I]
         lib.oracle_decode_e2m1.restype = ctypes.c_double
+        lib.oracle_decode_f16.argtypes = [I]
+        lib.oracle_decode_f16.restype = ctypes.c_double
         lib.oracle_paged_decode_attention_nvfp4.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I,
                                                             I, I, I, F, I, F, F, I]
         lib.oracle_paged_decode_attention_nvfp4.restype = I
@@ -89,8 +91,10 @@ def _dtype_code(a: np.ndarray) -> int:
         return ORC_BF16
     if a.dtype == np.uint8:
         return ORC_FP8_E4M3
-    raise TypeError("oracle takes float32, uint16 (bf16 bits) or uint8 (FP8 E4M3 codes) "
-                    f"arrays, got {a.dtype}")
+    if a.dtype == np.float16:
+        return ORC_F16
+    raise TypeError("oracle takes float32, float16, uint16 (bf16 bits) or uint8 (FP8 E4M3 "
+                    f"codes) arrays, got {a.dtype}")
 
 
 def _ptr(a: np.ndarray):
@@ -155,6 +159,11 @@ def paged_decode_attention_nvfp4(q, k_data, v_data, k_block_scales, v_block_scal
         ctypes.c_float(scale), _dtype_code(q), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
         int(num_threads))
     return out, st
+
+
+def decode_f16(bits: int, lib=None) -> float:
+    """The value of a binary16 bit pattern (exact in double)."""
+    return (lib or load()).oracle_decode_f16(int(bits))
 
 
 def decode_e4m3(code: int, lib=None) -> float:

@@ -25,7 +25,9 @@ Facts used:
     and to hand-derived values at the format's landmarks; FP8 attention with per-tensor
     scales matches the dense brute force run on torch-decoded, scaled values;
   - every FP4 E2M1 code decodes to the format's table of values; NVFP4 attention matches
-    the dense brute force run on values decoded through that table and torch's E4M3.
+    the dense brute force run on values decoded through that table and torch's E4M3;
+  - every binary16 bit pattern decodes to NumPy's float16 value, and to hand-derived values
+    at the format's landmarks; fp16 attention matches the dense brute force.
 """
 from __future__ import annotations
 
@@ -51,7 +53,11 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 def as_stored(x: np.ndarray, dtype: str) -> np.ndarray:
-    return f32_to_bf16_bits(x) if dtype == "bf16" else np.ascontiguousarray(x, np.float32)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    if dtype == "f16":  # NumPy's binary16 conversion (round to nearest even)
+        return np.ascontiguousarray(x, np.float32).astype(np.float16)
+    return np.ascontiguousarray(x, np.float32)
 
 
 def stored_to_f64(a: np.ndarray) -> np.ndarray:
@@ -181,7 +187,9 @@ def pin_brute_force(lib):
     cases = [([1, 17, 33, 100], 2, 2, 64, 16, "f32"),
              ([3, 8, 9, 0, 25], 4, 1, 16, 8, "bf16"),
              ([31, 2, 64], 8, 2, 32, 16, "bf16"),
-             ([7, 19], 6, 3, 8, 4, "f32")]
+             ([7, 19], 6, 3, 8, 4, "f32"),
+             ([5, 40, 16], 4, 2, 16, 16, "f16"),
+             ([2, 33], 8, 8, 8, 32, "f16")]
     for lengths, H, H_kv, D, bs, dtype in cases:
         p = Paged(rng, lengths, H=H, H_kv=H_kv, D=D, bs=bs, dtype=dtype)
         scale = float(np.float32(1.0 / math.sqrt(D)))
@@ -264,7 +272,7 @@ def pin_error_rows(lib):
 
 def pin_append_then_pack_roundtrip(lib):
     rng = np.random.default_rng(21)
-    for dtype in ("f32", "bf16"):
+    for dtype in ("f32", "bf16", "f16"):
         H_kv, D, bs = 2, 8, 4
         hist_len = [4, 6, 11]
         p = Paged(rng, [L + 1 for L in hist_len], H=2, H_kv=H_kv, D=D, bs=bs, dtype=dtype)
@@ -293,7 +301,7 @@ def pin_append_then_pack_roundtrip(lib):
 
 def pin_unpack_then_pack_roundtrip(lib):
     rng = np.random.default_rng(22)
-    for dtype in ("f32", "bf16"):
+    for dtype in ("f32", "bf16", "f16"):
         H_kv, D, bs = 2, 8, 4
         for L in (1, 4, 9, 13):
             NB = (L + bs - 1) // bs + 5
@@ -378,6 +386,23 @@ def pin_fp8_attention_brute_force(lib):
 
 # FP4 E2M1 magnitudes by 3-bit code (sign is the 4th bit), as the format lists them
 E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def pin_f16_decode(lib):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.decode_f16(int(b), lib=lib) for b in range(1 << 16)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+    # landmarks of the format, derived by hand
+    hand = {0x0000: 0.0, 0x3C00: 1.0, 0x3E00: 1.5, 0x4000: 2.0, 0x7BFF: 65504.0,
+            0x0400: 2.0 ** -14, 0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24, 0xC000: -2.0,
+            0x7C00: math.inf, 0xFC00: -math.inf, 0x3555: 1365 * 2.0 ** -12}
+    for b, v in hand.items():
+        assert orc.decode_f16(b, lib=lib) == v, hex(b)
+    assert np.isnan(orc.decode_f16(0x7E00, lib=lib)) and np.isnan(orc.decode_f16(0xFC01, lib=lib))
 
 
 def pin_e2m1_decode(lib):

@@ -61,6 +61,13 @@ MUTANTS = [
     ("nvfp4_nibbles_swapped",
      [("(d & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15)",
        "(d & 1) ? (unsigned)(byte & 15) : (unsigned)(byte >> 4)", None)]),
+    ("f16_wrong_exponent_bias",
+     [("mag = ldexp((double)(1024 + m), e - 25);", "mag = ldexp((double)(1024 + m), e - 24);",
+       None)]),
+    ("f16_subnormal_scale",
+     [("mag = ldexp((double)m, -24);", "mag = ldexp((double)m, -25);", None)]),
+    ("f16_sign_dropped", [("  return sign ? -mag : mag;\n}\n\ndouble oracle_decode_f16",
+                           "  return mag;\n}\n\ndouble oracle_decode_f16", None)]),
     ("nvfp4_wrong_block_index",
      [("srow * (size_t)(D / 16) + (size_t)(d / 16)", "srow * (size_t)(D / 16) + (size_t)(d / 32)",
        None)]),
