@@ -52,12 +52,20 @@ typedef enum {
   PDA_ERR_TOO_LARGE = 5    /* needs more scratch than pda_paged_decode_attention_noalloc has */
 } pda_status;
 
-/* Element types. PDA_FP8_E4M3 (the OCP 8-bit format without infinities) is a KV-cache type
- * only: append, pack and unpack copy its bytes, and pda_paged_decode_attention_fp8 reads it
- * with per-tensor scales. PDA_NVFP4 names the 4-bit cache read by
- * pda_paged_decode_attention_nvfp4 (and sizes its workspace); its data tensors are moved as
- * 1-byte rows by append, pack and unpack, its block scales by the *_block_scales calls. */
-typedef enum { PDA_F32 = 0, PDA_BF16 = 1, PDA_FP8_E4M3 = 2, PDA_NVFP4 = 3 } pda_dtype;
+/* Element types. PDA_F32, PDA_BF16 and PDA_F16 (IEEE binary16, the precision the pages'
+ * decode kernels were measured in) are q, output and KV-cache types. PDA_FP8_E4M3 (the OCP
+ * 8-bit format without infinities) is a KV-cache type only: append, pack and unpack copy
+ * its bytes, and pda_paged_decode_attention_fp8 reads it with per-tensor scales. PDA_NVFP4
+ * names the 4-bit cache read by pda_paged_decode_attention_nvfp4 (and sizes its workspace);
+ * its data tensors are moved as 1-byte rows by append, pack and unpack, its block scales by
+ * the *_block_scales calls. */
+typedef enum {
+  PDA_F32 = 0,
+  PDA_BF16 = 1,
+  PDA_FP8_E4M3 = 2,
+  PDA_NVFP4 = 3,
+  PDA_F16 = 4
+} pda_dtype;
 
 /* Bits OR-ed into *error_word by the kernels. */
 #define PDA_DEVERR_CONTEXT_LEN 0x1 /* context_lens[b] < 0, > max_context_len or > table capacity */
@@ -130,10 +138,11 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  * Orca's iteration-level batching, page "Disaggregated LLM Serving", sec. 2.1, applied
  * also along the sequence). Accumulation is fp32.
  *
- *  out            [B, H, D] in out_dtype (PDA_F32 or PDA_BF16).
+ *  out            [B, H, D] in out_dtype (PDA_F32, PDA_BF16 or PDA_F16).
  *  q              [B, H, D] in q_dtype; q_dtype must equal kv_dtype.
- *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype (PDA_F32 or PDA_BF16; an
- *                 FP8 cache goes through pda_paged_decode_attention_fp8); read only.
+ *  k_cache,v_cache [num_blocks, block_size, H_kv, D] in kv_dtype (PDA_F32, PDA_BF16 or
+ *                 PDA_F16; an FP8 cache goes through pda_paged_decode_attention_fp8); read
+ *                 only.
  *  block_tables   [B, max_blocks_per_seq] int32.
  *  context_lens   [B] int32 (device): tokens of history including this step's token.
  *                 L == 0 gives a zero row. L < 0, L > max_context_len or
@@ -154,7 +163,7 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  *                 the workspace before the next replay.)
  *  Supported: D in {64, 128}; block_size in {16, 32, 64, 128, 256} (the kernel works in
  *  tiles of 16 rows of one physical block); H / H_kv in {1, 2, 4, 8}; B <= 8192;
- *  kv_dtype in {PDA_F32, PDA_BF16}. Pointers 16-byte aligned. Other sizes return
+ *  kv_dtype in {PDA_F32, PDA_BF16, PDA_F16}. Pointers 16-byte aligned. Other sizes return
  *  PDA_ERR_UNSUPPORTED.
  */
 pda_status pda_paged_decode_attention(void* out, const void* q, const void* k_cache,

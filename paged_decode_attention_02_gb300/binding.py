@@ -17,7 +17,7 @@ from . import build_lib
 
 (PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED, PDA_ERR_CUDA, PDA_ERR_WORKSPACE,
  PDA_ERR_TOO_LARGE) = range(6)
-PDA_F32, PDA_BF16, PDA_FP8_E4M3, PDA_NVFP4 = 0, 1, 2, 3
+PDA_F32, PDA_BF16, PDA_FP8_E4M3, PDA_NVFP4, PDA_F16 = 0, 1, 2, 3, 4
 PDA_DEVERR_CONTEXT_LEN, PDA_DEVERR_BLOCK_ID, PDA_DEVERR_SLOT, PDA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PDA_PACK_MAX_BATCH = 64
 PDA_PACK_MAX_LAYERS = 256
@@ -139,14 +139,18 @@ def _check(status: int, what: str):
 
 
 def _dtype(t: torch.Tensor) -> int:
-    """float32, bfloat16, or FP8 E4M3 codes (torch.float8_e4m3fn, or uint8 holding codes)."""
+    """float32, bfloat16, float16, or FP8 E4M3 codes (torch.float8_e4m3fn, or uint8 holding
+    codes)."""
     if t.dtype == torch.float32:
         return PDA_F32
     if t.dtype == torch.bfloat16:
         return PDA_BF16
+    if t.dtype == torch.float16:
+        return PDA_F16
     if t.dtype in (torch.uint8, torch.float8_e4m3fn):
         return PDA_FP8_E4M3
-    raise TypeError(f"unsupported dtype {t.dtype}; use float32, bfloat16 or FP8 E4M3 codes")
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32, bfloat16, float16 or FP8 E4M3 "
+                    "codes")
 
 
 def _ptr(t: torch.Tensor | None):
@@ -184,8 +188,8 @@ def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, error_word=None, str
 def attention_workspace_size(B, H, H_kv, D, block_size=16, kv_dtype=torch.bfloat16,
                              sm_cap=0) -> int:
     n = ctypes.c_size_t(0)
-    dt = {torch.bfloat16: PDA_BF16, torch.float32: PDA_F32, torch.uint8: PDA_FP8_E4M3,
-          torch.float8_e4m3fn: PDA_FP8_E4M3}[kv_dtype]
+    dt = {torch.bfloat16: PDA_BF16, torch.float32: PDA_F32, torch.float16: PDA_F16,
+          torch.uint8: PDA_FP8_E4M3, torch.float8_e4m3fn: PDA_FP8_E4M3}[kv_dtype]
     _check(load().pda_attention_workspace_size(B, H, H_kv, D, block_size, dt, sm_cap,
                                                ctypes.byref(n)), "pda_attention_workspace_size")
     return n.value

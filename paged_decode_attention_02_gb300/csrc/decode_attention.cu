@@ -114,7 +114,7 @@ struct AttnParams {
   int B, H, H_kv, num_blocks, max_blocks, max_context_len;
   int block_size;                 // tokens per physical block: 16 << bs_shift
   int bs_shift;                   // log2 of the 16-row tiles per physical block
-  int out_bf16;
+  int out_kind;                   // output type: 0 fp32, 1 bf16, 2 fp16
   float scale_log2;
   int num_workers;
   int stages;
@@ -404,9 +404,31 @@ __device__ __forceinline__ void store_f32(float* p, const float* v, int n) {
     *reinterpret_cast<float4*>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
 }
 
+// Output kinds (AttnParams::out_kind).
+constexpr int kOutF32 = 0;
+constexpr int kOutBF16 = 1;
+constexpr int kOutF16 = 2;
+
+__device__ __forceinline__ void store_one(void* out, size_t off, float v, int kind) {
+  if (kind == kOutBF16)
+    reinterpret_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(v);
+  else if (kind == kOutF16)
+    reinterpret_cast<__half*>(out)[off] = __float2half_rn(v);
+  else
+    reinterpret_cast<float*>(out)[off] = v;
+}
+
 __device__ __forceinline__ void store_out(void* out, size_t off, const float* v, int n,
-                                          int out_bf16) {
-  if (out_bf16) {
+                                          int kind) {
+  if (kind == kOutF16) {
+    __half* p = reinterpret_cast<__half*>(out) + off;
+    if (n % 2 == 0) {
+      for (int e = 0; e < n; e += 2)
+        *reinterpret_cast<__half2*>(p + e) = __floats2half2_rn(v[e], v[e + 1]);
+    } else {
+      for (int e = 0; e < n; ++e) p[e] = __float2half_rn(v[e]);
+    }
+  } else if (kind == kOutBF16) {
     __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + off;
     if (n == 2) {
       *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
@@ -539,10 +561,7 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const float v = acc[j][e] * (p.v_scale / Lsum[j]);
-      if (p.out_bf16)
-        reinterpret_cast<__nv_bfloat16*>(p.out)[row + lane + 32 * e] = __float2bfloat16_rn(v);
-      else
-        reinterpret_cast<float*>(p.out)[row + lane + 32 * e] = v;
+      store_one(p.out, row + lane + 32 * e, v, p.out_kind);
     }
   }
 }
@@ -650,10 +669,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
     const float val = bad ? __int_as_float(0x7fc00000) : 0.f;
     for (int i = tid; i < p.H * D; i += blockDim.x) {
       const size_t off = static_cast<size_t>(b) * p.H * D + i;
-      if (p.out_bf16)
-        reinterpret_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(val);
-      else
-        reinterpret_cast<float*>(p.out)[off] = val;
+      store_one(p.out, off, val, p.out_kind);
     }
   }
 
@@ -851,7 +867,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
             if (e < n) v[e] = o[e] * inv;
           const size_t off =
               (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D + d;
-          store_out(p.out, off, v, n, p.out_bf16);
+          store_out(p.out, off, v, n, p.out_kind);
         });
       } else {
         // A piece of a segment cut by a range boundary: store (m, l, o), register it, and
@@ -1025,7 +1041,10 @@ KernelFn pick_g(int G_u, int mode) {
 }
 
 KernelFn pick_kernel(pda_dtype kv, int D, const Tiling& t) {
-  if (kv == PDA_BF16) {
+  if (kv == PDA_F16) {
+    if (D == 128) return pick_g<__half, __half, 128>(t.G_u, t.mode);
+    if (D == 64) return pick_g<__half, __half, 64>(t.G_u, t.mode);
+  } else if (kv == PDA_BF16) {
     if (D == 128) return pick_g<__nv_bfloat16, __nv_bfloat16, 128>(t.G_u, t.mode);
     if (D == 64) return pick_g<__nv_bfloat16, __nv_bfloat16, 64>(t.G_u, t.mode);
   } else if (kv == PDA_FP8_E4M3) {
@@ -1227,7 +1246,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.block_size = block_size;
   ap.bs_shift = 0;
   while ((kBS << ap.bs_shift) < block_size) ++ap.bs_shift;
-  ap.out_bf16 = out_dtype == PDA_BF16;
+  ap.out_kind = out_dtype == PDA_BF16 ? kOutBF16 : out_dtype == PDA_F16 ? kOutF16 : kOutF32;
   // the K scale folds into q's pre-scale: s = scale * (k_scale * code) . q
   ap.scale_log2 = scale * k_scale * 1.4426950408889634f;
   ap.num_workers = pl.grid * pl.nwarps;

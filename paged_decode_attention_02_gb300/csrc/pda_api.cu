@@ -62,6 +62,7 @@ pda_status encode_kv_tensor_map(CUtensorMap* tm, const void* base, int num_block
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   const CUtensorMapDataType dt = dtype == PDA_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == PDA_F16      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                  : dtype == PDA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   // With a swizzle the row (box width) must equal the swizzle span: 16-byte chunk c of

@@ -194,6 +194,23 @@ struct Elem<__nv_bfloat16> {
   }
 };
 
+template <>
+struct Elem<__half> {
+  static constexpr int kBits = 16;
+  static constexpr int kBytes = 2;
+  static constexpr int kVec = 8;  // one 16-byte access
+  static __device__ __forceinline__ void load(const void* p, float* out) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      out[2 * i] = f.x;
+      out[2 * i + 1] = f.y;
+    }
+  }
+};
+
 // Four E4M3 codes in a 32-bit word, widened exactly (E4M3 values are all exact in fp16).
 __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* out) {
   uint32_t h01, h23;

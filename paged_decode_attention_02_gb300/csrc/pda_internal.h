@@ -32,12 +32,14 @@ pda_status encode_kv_pair_tensor_map(CUtensorMap* tm, const void* base, int num_
                                      int swizzle_bytes, int box_rows);
 
 inline size_t dtype_bytes(pda_dtype t) {
-  return t == PDA_BF16 ? 2u : (t == PDA_FP8_E4M3 ? 1u : 4u);
+  return (t == PDA_BF16 || t == PDA_F16) ? 2u : (t == PDA_FP8_E4M3 ? 1u : 4u);
 }
 // Types a KV cache may hold.
-inline bool dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16 || t == PDA_FP8_E4M3; }
+inline bool dtype_ok(int t) {
+  return t == PDA_F32 || t == PDA_BF16 || t == PDA_F16 || t == PDA_FP8_E4M3;
+}
 // Types of q and out.
-inline bool float_dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16; }
+inline bool float_dtype_ok(int t) { return t == PDA_F32 || t == PDA_BF16 || t == PDA_F16; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

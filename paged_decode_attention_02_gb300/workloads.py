@@ -19,7 +19,7 @@ Recipe (one per named workload):
     entries are -1;
   - q, the pool's K and V, and the appended token's K/V are N(0,1) drawn in fp32 by a
     ``torch.Generator`` seeded from the third stream, on the device the caller asks for,
-    then rounded to the workload's dtype (round-to-nearest-even for bf16);
+    then rounded to the workload's dtype (round-to-nearest-even for bf16 and fp16);
   - FP8 workloads store E4M3 codes of value / scale (per-tensor scales, K and V apart;
     torch's float8_e4m3fn rounding), drawn with the seeds of their bf16 twin so the
     lengths and tables are the same;
@@ -49,7 +49,7 @@ class Workload:
     H_kv: int
     D: int
     block_size: int
-    dtype: str  # "f32" or "bf16": q, K/V and output
+    dtype: str  # "f32", "bf16" or "f16": q, K/V and output
     lengths: str  # recipe name, see draw_lengths
     pool: str  # "fixed:<n>" or "scaled:<factor>"
     pack_top: int = 0  # number of longest requests whose KV is packed each step
@@ -66,7 +66,7 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
 
     @property
     def elem_bytes(self) -> int:

@@ -120,6 +120,8 @@ SHAPES = [  # (dtype, D, H, H_kv)
     ("bf16", 128, 12, 3), ("bf16", 128, 7, 7), ("bf16", 128, 16, 2),
     ("bf16", 64, 16, 16), ("bf16", 64, 16, 8), ("bf16", 64, 16, 4), ("bf16", 64, 16, 2),
     ("f32", 64, 8, 8), ("f32", 64, 8, 2), ("f32", 128, 8, 8), ("f32", 128, 16, 2),
+    ("f16", 128, 32, 8), ("f16", 128, 40, 40), ("f16", 128, 12, 3), ("f16", 64, 16, 4),
+    ("f16", 64, 8, 8),
 ]
 
 
@@ -143,6 +145,20 @@ def test_bf16_inputs_fp32_output():
     out, err = gpu_step(s, out_dtype=torch.float32)
     assert err == 0
     assert_attention_close(out, ref, "bf16 in, f32 out")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.float32])
+def test_fp16_step_every_output(out_dtype):
+    """fp16 q and caches (the precision the pages' decode kernels ran in), fp16 or fp32
+    output, GQA and MHA, with the longest requests split over several workers."""
+    for base in ("gqa_skew_b256", "llama2_13b_b80"):
+        s = wl.make_step(variant(base, dtype="f16", B=16), device=DEV)
+        ref, st, kc, vc = oracle_full_step(s)
+        assert st == 0
+        out, err = gpu_step(s, out_dtype=out_dtype)
+        assert err == 0
+        assert np.array_equal(to_np(s.k_cache).view(np.uint8), kc.view(np.uint8))
+        assert_attention_close(out, ref, f"{base} fp16 -> {out_dtype}", strict=True)
 
 
 # ------------------------------------------------------------------ edge cases
@@ -738,7 +754,7 @@ def test_quantised_single_very_long_request_split_over_every_worker(name):
 # block holding block_size / 16 of them; append and pack move whole rows whatever the size.
 BLOCK_SIZE_CASES = [("gqa_skew_b256", {}), ("llama2_13b_b80", {}),
                     ("llama2_13b_b80", {"D": 64, "H": 16, "H_kv": 4}),
-                    ("tiny", {}),
+                    ("tiny", {}), ("gqa_skew_b256", {"dtype": "f16"}),
                     ("gqa_skew_b256_fp8", {}), ("gqa_skew_b256_nvfp4", {}),
                     ("llama2_13b_b80_nvfp4", {}), ("gqa_skew_b256_nvfp4", {"H": 12, "H_kv": 3})]
 
