@@ -663,7 +663,8 @@ def sweep_workloads(args, dev, flush, peak):
     sms = pda.device_sm_count()
     stream = torch.cuda.current_stream(dev)
     for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
-                 "gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4", "gqa_skew_b256_nvfp4"):
+                 "gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4", "gqa_skew_b256_nvfp4",
+                 "gqa_skew_b256_f16", "gqa_skew_b256_bs64"):
         if name == args.config:
             continue
         w = wl.get(name)

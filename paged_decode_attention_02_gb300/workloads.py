@@ -121,6 +121,12 @@ WORKLOADS = {
                  dtype="bf16", lengths="uniform:128,4096", pool="scaled:1.25", kv="nvfp4",
                  k_scale=0.9, v_scale=1.3, seed_of=3,
                  description="llama2_13b_b80 with an NVFP4 KV cache"),
+        Workload("gqa_skew_b256_f16", 10, B=256, H=32, H_kv=8, D=128, block_size=16,
+                 dtype="f16", lengths="loguniform:16,32768", pool="scaled:1.25", pack_top=8,
+                 seed_of=4, description="gqa_skew_b256 in fp16 (q, caches and output)"),
+        Workload("gqa_skew_b256_bs64", 11, B=256, H=32, H_kv=8, D=128, block_size=64,
+                 dtype="bf16", lengths="loguniform:16,32768", pool="scaled:1.25", pack_top=8,
+                 seed_of=4, description="gqa_skew_b256 over 64-token physical blocks"),
     ]
 }
 

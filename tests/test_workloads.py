@@ -7,10 +7,10 @@ from paged_decode_attention_02_gb300 import workloads as wl
 
 
 def test_named_workloads():
-    assert [wl.get(i).name for i in range(1, 10)] == [
+    assert [wl.get(i).name for i in range(1, 12)] == [
         "tiny", "llama2_7b_b8", "llama2_13b_b80", "gqa_skew_b256", "sm_sweep_b128",
         "gqa_skew_b256_fp8", "llama2_13b_b80_fp8", "gqa_skew_b256_nvfp4",
-        "llama2_13b_b80_nvfp4"]
+        "llama2_13b_b80_nvfp4", "gqa_skew_b256_f16", "gqa_skew_b256_bs64"]
 
 
 def test_nvfp4_workload_has_codes_and_block_scales():
