@@ -46,7 +46,7 @@ extern "C" {
 typedef enum {
   PDA_OK = 0,
   PDA_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size, misalignment */
-  PDA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+  PDA_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement */
   PDA_ERR_CUDA = 3,        /* a CUDA runtime call failed; see cudaGetLastError */
   PDA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
   PDA_ERR_TOO_LARGE = 5    /* needs more scratch than pda_paged_decode_attention_noalloc has */
