@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 HEADLINE = "gqa_skew_b256"
 METRIC = "paged decode-attn HBM GB/s (% of GB300 peak) and decode tokens/s per layer"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300's HBM3e rate as the task names it (~8 TB/s)
 ATTN_SOURCES = ["paged_decode_attention_02_gb300/csrc/decode_attention.cu",
                 "paged_decode_attention_02_gb300/csrc/pda_device.cuh",
                 "paged_decode_attention_02_gb300/csrc/warp_attn_tc.cuh",
@@ -90,18 +91,21 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+def profiled_traffic(workload: str, algorithmic_bytes: int):
+    """DRAM bytes per full-size attention launch, from the committed ncu summary of the
+    workload if it was taken on the current kernel source, else None. The capture runs a
+    reduced batch of the same recipe (a few GB on the device at most); its DRAM bytes over
+    its algorithmic bytes (``dram_traffic_ratio``) scale the full launch's algorithmic bytes,
+    since both grow with the tokens streamed."""
     path = os.path.join(ROOT, "profiles", f"attn_partial_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text)
-    m_b = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != kernel_sha():
+    m_r = re.search(r"dram_traffic_ratio:\s*([0-9.]+)", text)
+    if not m_sha or not m_r or m_sha.group(1) != kernel_sha():
         return None
-    return float(m_b.group(1))
+    return int(round(float(m_r.group(1)) * algorithmic_bytes))
 
 
 # ------------------------------------------------------------------ clocks
@@ -485,7 +489,8 @@ def run_ours(args, ws, rank, local):
 
     peak, peak_src = hbm_peak()
     attn_gbs = nb["attention"] / t_attn / 1e9
-    traffic = profiled_traffic(w.name) if (args.batch is None and cap == 0) else None
+    traffic = (profiled_traffic(w.name, nb["attention"])
+               if (args.batch is None and cap == 0) else None)
     res = {
         "metric": METRIC,
         "value": round(replica_value(nb["step"], t_step_max, ws), 2),
@@ -537,6 +542,7 @@ def run_ours(args, ws, rank, local):
     if args.sweeps and ws == 1:
         res["workloads"] = sweep_workloads(args, dev, flush, peak)
         res["kv_transfer_staging"] = transfer_legs(dev)
+    res["per_config"] = per_config(w, s.B, res["attention"], res.get("workloads"), peak)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
         sample = oracle_sample(w, args.cpu_seconds, threads)
@@ -555,6 +561,41 @@ def run_ours(args, ws, rank, local):
                       f"{threads} threads in {t_cpu:.1f} s; one pass on 1 thread in "
                       f"{t_one:.1f} s"}
     return res
+
+
+def per_config(w, B, headline_attn, workloads, peak) -> dict:
+    """Attention alone on each named workload, compact: us per layer (one attention launch),
+    decode tokens/s per layer (B / t), algorithmic GB/s, and its fraction of the measured
+    copy peak and of the nominal 8 TB/s HBM3e rate; the SM-fraction workload at each cap."""
+    from paged_decode_attention_02_gb300 import workloads as wl
+
+    def entry(r):
+        return {"us": r["us"], "tok_s": r["decode_tokens_per_s_per_layer"], "GBps": r["GBps"],
+                "frac": r["frac_of_peak"], "frac_8TB": round(r["GBps"] / NOMINAL_HBM_GBS, 4)}
+
+    res = {"peak_GBps": peak, "nominal_GBps": NOMINAL_HBM_GBS}
+    res[w.name] = dict(entry(headline_attn), B=B)
+    for name, r in (workloads or {}).items():
+        caps = wl.get(name).sm_caps_pct
+        if not caps:
+            res[name] = entry(r["all_sms"])
+            continue
+        sub = {}
+        for key, v in r.items():
+            if key == "all_sms":
+                sub["100%"] = entry(v)
+            elif key.startswith("sm_cap_"):
+                n = int(key[len("sm_cap_"):])
+                pct = [p for p in caps if p < 100 and math.ceil(p / 100 * _sms()) == n]
+                sub[f"{pct[0] if pct else '?'}% ({n} SMs)"] = dict(entry(v), GBps_per_SM=round(
+                    v["GBps"] / n, 1))
+        res[name] = sub
+    return res
+
+
+def _sms() -> int:
+    import paged_decode_attention_02_gb300 as pda
+    return pda.device_sm_count()
 
 
 def transfer_legs(dev, n_layers: int = 40, prompts=(2048, 8192), reps: int = 5) -> dict:
@@ -662,7 +703,7 @@ def sweep_workloads(args, dev, flush, peak):
     out_all = {}
     sms = pda.device_sm_count()
     stream = torch.cuda.current_stream(dev)
-    for name in ("llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
+    for name in ("tiny", "llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
                  "gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4", "gqa_skew_b256_nvfp4",
                  "gqa_skew_b256_f16", "gqa_skew_b256_bs64"):
         if name == args.config:
@@ -872,6 +913,13 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    launched = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != launched:
+        print(f"bench.py --gpus {args.gpus}: one process per GPU is needed; launch it as "
+              f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py "
+              f"--gpus {args.gpus} ... (this process sees WORLD_SIZE={launched})",
+              file=sys.stderr)
+        sys.exit(2)
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, ws, rank)

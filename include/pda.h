@@ -158,9 +158,11 @@ pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D, int block
  *  workspace      device scratch of at least pda_attention_workspace_size(...) bytes,
  *                 256-byte aligned; not shared by calls that may run concurrently. No
  *                 initialisation is needed: its arrival counters are tagged with a number
- *                 the library gives each call. (A call captured in a CUDA graph keeps its
- *                 number on every replay; if a replay ever reports PDA_DEVERR_TIMEOUT, zero
- *                 the workspace before the next replay.)
+ *                 the library gives each call, mixed with a fixed 48-bit pattern so that
+ *                 what another call left there (zeros, or the fp32 partial results of a call
+ *                 of another shape) is not taken for a live counter. (A call captured in a
+ *                 CUDA graph keeps its number on every replay; if a replay ever reports
+ *                 PDA_DEVERR_TIMEOUT, zero the workspace before the next replay.)
  *  Supported: D in {64, 128}; block_size in {16, 32, 64, 128, 256} (the kernel works in
  *  tiles of 16 rows of one physical block); H / H_kv in {1, 2, 4, 8}; B <= 8192;
  *  kv_dtype in {PDA_F32, PDA_BF16, PDA_F16}. Pointers 16-byte aligned. Other sizes return
@@ -270,10 +272,12 @@ pda_status pda_paged_decode_attention_nvfp4(void* out, const void* q, const void
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *    with that device current) and caches it; make that first call before any stream
  *    capture on that device.
- *  - Every call shares the one array, which keeps the previous call's contents. Nothing in
- *    it needs to start at zero: partial results are written before they are read, and the
- *    per-segment arrival counters carry the number of the call that last wrote them, so
- *    values left by an earlier call are recognised as stale.
+ *  - Every call shares the one array, which keeps the previous call's contents: those of a
+ *    call of another shape, or of one that stopped early with PDA_DEVERR_TIMEOUT. Partial
+ *    results are written before they are read. The per-segment arrival counters at the
+ *    head of the array must not carry counts from an earlier call, so every call first
+ *    clears them (B * H_kv * 8 bytes or less, one cudaMemsetAsync on `stream`, which
+ *    allocates nothing) and then launches the kernel.
  *    Calls that overlap on the GPU (on different streams, or from different host threads)
  *    race on the array and produce wrong results; serialise them.
  */

@@ -451,15 +451,26 @@ __device__ __forceinline__ void store_out(void* out, size_t off, const float* v,
   }
 }
 
+// Arrival counters hold ((call number << 16) | count) ^ kTagMix. A counter written by an
+// earlier call (or one that was aborted) carries another call number and counts as 0. The
+// mix keeps other data from passing for a live counter: a workspace reused for calls of
+// other shapes holds fp32 partial results where this call's counters lie, and zeros or
+// small values there would otherwise read as the tag of one of the first calls.
+constexpr unsigned long long kTagMix = 0xa5c396e17b2d0000ull;
+
+__device__ __forceinline__ unsigned long long arrival_reset(unsigned long long call) {
+  return (call << 16) ^ kTagMix;
+}
+
 // Registers one more piece of a segment and returns how many pieces of it this call has
-// registered so far. The counter holds (call number << 16) | count; a counter written by
-// an earlier call (or one that was aborted) carries another call number and counts as 0.
+// registered so far.
 __device__ __forceinline__ unsigned arrive(unsigned long long* counter,
                                            unsigned long long call) {
   unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
   while (true) {
-    const unsigned long long next = ((old >> 16) == call) ? old + 1 : ((call << 16) | 1ull);
-    const unsigned long long seen = atomicCAS(counter, old, next);
+    const unsigned long long cur = old ^ kTagMix;
+    const unsigned long long next = ((cur >> 16) == call) ? cur + 1 : ((call << 16) | 1ull);
+    const unsigned long long seen = atomicCAS(counter, old, next ^ kTagMix);
     if (seen == old) return static_cast<unsigned>(next & 0xffffull);
     old = seen;
   }
@@ -902,7 +913,7 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
           __threadfence();  // see the other pieces' stores
           merge_segment<D, G>(p, cb, ch, w0, w1, seg_start != tile_start(w0, W_tiles, NW),
                               W_tiles, NW, lane);
-          if (lane == 0) atomicExch(p.ws_arrive + seg, p.call << 16);
+          if (lane == 0) atomicExch(p.ws_arrive + seg, arrival_reset(p.call));
         }
       }
     }
@@ -1167,7 +1178,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
                             float k_scale, float v_scale, pda_dtype q_dtype,
                             pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
                             void* workspace, size_t workspace_bytes, int32_t* error_word,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool clear_arrivals = false) {
   // ---- host-side validation, before any CUDA call
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || sm_cap < 0 ||
@@ -1254,6 +1265,12 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.stage_bytes = pl.stage_bytes;
   ap.prefix_bytes = pl.prefix_bytes;
 
+  // clear_arrivals: zero the arrival counters first (a memset on the same stream), so no
+  // counter left in the workspace by an earlier call can pass for one of this call's
+  if (clear_arrivals &&
+      cudaMemsetAsync(ap.ws_arrive, 0, static_cast<size_t>(B) * tiling.H_u * 8, stream) !=
+          cudaSuccess)
+    return PDA_ERR_CUDA;
   fn<<<pl.grid, pl.nwarps * 32, pl.smem_bytes, stream>>>(tmK, tmV, ap);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   return PDA_OK;
@@ -1339,6 +1356,7 @@ extern "C" pda_status pda_paged_decode_attention_noalloc(
     int max_context_len, int B, int H, int H_kv, int D, int block_size, int num_blocks,
     float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
     int32_t* error_word, cudaStream_t stream) {
+  if (kv_dtype == PDA_FP8_E4M3) return PDA_ERR_UNSUPPORTED;  // as pda_paged_decode_attention
   size_t need = 0;
   pda_status st = pda_attention_workspace_size(B, H, H_kv, D, block_size, kv_dtype, sm_cap,
                                                &need);
@@ -1349,8 +1367,11 @@ extern "C" pda_status pda_paged_decode_attention_noalloc(
   void* scratch = nullptr;
   st = noalloc_scratch(dev, &scratch);
   if (st != PDA_OK) return st;
-  return pda_paged_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                    context_lens, max_context_len, B, H, H_kv, D, block_size,
-                                    num_blocks, scale, q_dtype, kv_dtype, out_dtype, sm_cap,
-                                    scratch, PDA_NOALLOC_SCRATCH_BYTES, error_word, stream);
+  // The shared array keeps whatever the previous call left, which may be a call of another
+  // shape or one that timed out: its counters are cleared before the kernel runs.
+  return launch_attention(out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, B, H, H_kv, D,
+                          block_size, num_blocks, scale, 1.f, 1.f, q_dtype, kv_dtype, out_dtype,
+                          sm_cap, scratch, PDA_NOALLOC_SCRATCH_BYTES, error_word, stream,
+                          /*clear_arrivals=*/true);
 }

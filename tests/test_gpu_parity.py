@@ -6,14 +6,15 @@ the full-size workloads, in the launch configuration the benchmark times, compar
 requests (longest, shortest and random ones) that the oracle computes one by one.
 """
 import dataclasses
+import math
 
 import numpy as np
 import pytest
 import torch
 
 import paged_decode_attention_02_gb300 as pda
-from gpu_common import (assert_attention_close, gpu_step, oracle_full_step, oracle_sampled,
-                        to_np)
+from gpu_common import (assert_attention_close, fp32_twin, gpu_step, oracle_full_step,
+                        oracle_sampled, to_np)
 from oracle import oracle as orc
 from paged_decode_attention_02_gb300 import binding
 from paged_decode_attention_02_gb300 import workloads as wl
@@ -89,7 +90,55 @@ def test_full_size_sampled(name):
     assert torch.isfinite(out.float()).all()
 
 
+_FULL = {}
+
+
+def _full_step(name):
+    """A full-size step of workload ``name`` with the oracle of its sampled requests, shared
+    by the capped tests below (one pool on the device at a time). Each GPU step repeats the
+    append, which rewrites the same slots with the same values, so the caches stay as the
+    oracle saw them."""
+    if name not in _FULL:
+        _FULL.clear()
+        s = wl.make_step(name, device=DEV)
+        reqs = _sample(s)
+        ref, st = oracle_sampled(s, reqs)
+        assert st == 0
+        _FULL[name] = (s, reqs, ref)
+    return _FULL[name]
+
+
+def _cap(pct):
+    """The SM cap of the benchmark's sweep: ceil(pct % of the SMs)."""
+    return int(math.ceil(pct / 100 * pda.device_sm_count()))
+
+
+@pytest.mark.parametrize("pct", [10, 20, 40, 60])
+def test_sm_sweep_full_size_capped_sampled(pct):
+    """The SM-fraction sweep at its full 128 requests in the launches the benchmark times:
+    4096 (request, kv-head) segments cut over a few hundred workers and merged."""
+    s, reqs, ref = _full_step("sm_sweep_b128")
+    cap = _cap(pct)
+    out, err = gpu_step(s, sm_cap=cap)
+    assert err == 0
+    assert_attention_close(out[reqs], ref, f"sm_sweep_b128 sm_cap={cap}", strict=True)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "gqa_skew_b256_nvfp4"])
+def test_quantised_full_size_capped_sampled(name):
+    """The quantised GQA workloads at full size on 10 % of the SMs (two-kv-head tiles, every
+    long segment cut over many workers)."""
+    s, reqs, ref = _full_step(name)
+    cap = _cap(10)
+    out, err = gpu_step(s, sm_cap=cap)
+    assert err == 0
+    assert_attention_close(out[reqs], ref, f"{name} sm_cap={cap}", strict=True)
+    assert torch.isfinite(out.float()).all()
+
+
 def test_full_size_pack_of_longest_requests():
+    _FULL.clear()
     s = wl.make_step("gqa_skew_b256", device=DEV)
     reqs = s.pack_requests
     assert len(reqs) == 8
@@ -136,7 +185,7 @@ def test_shapes_and_groups(dtype, D, H, H_kv):
     out, err = gpu_step(s)
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc)
-    assert_attention_close(out, ref, f"{dtype} D={D} H={H} H_kv={H_kv}")
+    assert_attention_close(out, ref, f"{dtype} D={D} H={H} H_kv={H_kv}", twin=fp32_twin(s))
 
 
 def test_bf16_inputs_fp32_output():
@@ -169,11 +218,7 @@ def test_empty_and_single_token_histories():
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, "empty/single")
-    s2 = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=7)
-    out32, err = gpu_step(s2, out_dtype=torch.float32)
-    assert err == 0
-    assert_attention_close(out32, ref, "empty/single, fp32 output")
+    assert_attention_close(out, ref, "empty/single", twin=fp32_twin(s))
     assert (out[lens == 0] == 0).all()
     for b in np.where(lens == 1)[0]:
         assert torch.equal(out[b], s.v_new[b].to(out.dtype))  # exact: p = 1
@@ -192,7 +237,7 @@ def test_single_very_long_request_split_over_every_worker():
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, "B=1 L=32768")
+    assert_attention_close(out, ref, "B=1 L=32768", twin=fp32_twin(s))
 
 
 def test_many_one_block_requests():
@@ -203,11 +248,7 @@ def test_many_one_block_requests():
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, "600 one-block requests")
-    s2 = wl.make_step(w, device=DEV, lengths=lens)
-    out32, err = gpu_step(s2, out_dtype=torch.float32)
-    assert err == 0
-    assert_attention_close(out32, ref, "600 one-block requests, fp32 output")
+    assert_attention_close(out, ref, "600 one-block requests", twin=fp32_twin(s))
 
 
 def test_unused_rows_poisoned_with_nan_are_never_read():
@@ -217,7 +258,7 @@ def test_unused_rows_poisoned_with_nan_are_never_read():
     assert st == 0 and np.isfinite(ref).all()
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert_attention_close(out, ref, "poisoned")
+    assert_attention_close(out, ref, "poisoned", twin=fp32_twin(s))
 
 
 def test_shared_prefix_blocks_give_identical_rows():
@@ -233,7 +274,7 @@ def test_shared_prefix_blocks_give_identical_rows():
     assert np.array_equal(ref[0], ref[1])
     # The two rows may be split at different worker boundaries, so they can differ in the
     # fp32 summation order; both must match the (identical) oracle rows.
-    assert_attention_close(out, ref, "shared prefix")
+    assert_attention_close(out, ref, "shared prefix", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("cap", [1, 2, 15, 30, 61, 91, 152, 1000])
@@ -242,7 +283,7 @@ def test_sm_cap_does_not_change_results(cap):
     ref, _, _, _ = oracle_full_step(s)
     out, err = gpu_step(s, sm_cap=cap)
     assert err == 0
-    assert_attention_close(out, ref, f"sm_cap={cap}")
+    assert_attention_close(out, ref, f"sm_cap={cap}", twin=fp32_twin(s, cap))
 
 
 def test_repeat_runs_are_bitwise_identical():
@@ -452,7 +493,7 @@ def test_fp8_shapes_and_groups(D, H, H_kv):
     out, err = gpu_step(s)
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
-    assert_attention_close(out, ref, f"fp8 D={D} H={H} H_kv={H_kv}")
+    assert_attention_close(out, ref, f"fp8 D={D} H={H} H_kv={H_kv}", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("name,B", [("llama2_13b_b80_fp8", 10), ("gqa_skew_b256_fp8", 24)])
@@ -492,7 +533,7 @@ def test_fp8_empty_single_and_poisoned_rows():
     assert st == 0 and np.isfinite(ref).all()
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert_attention_close(out, ref, "fp8 edge cases")
+    assert_attention_close(out, ref, "fp8 edge cases", twin=fp32_twin(s))
     assert (out[0] == 0).all()
 
 
@@ -524,7 +565,7 @@ def test_nvfp4_shapes_and_groups(D, H, H_kv):
     assert err == 0
     assert np.array_equal(to_np(s.k_cache), kc) and np.array_equal(to_np(s.v_cache), vc)
     assert np.array_equal(to_np(s.k_bscales), ksc) and np.array_equal(to_np(s.v_bscales), vsc)
-    assert_attention_close(out, ref, f"nvfp4 D={D} H={H} H_kv={H_kv}")
+    assert_attention_close(out, ref, f"nvfp4 D={D} H={H} H_kv={H_kv}", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("name,B", [("llama2_13b_b80_nvfp4", 10), ("gqa_skew_b256_nvfp4", 24)])
@@ -554,7 +595,7 @@ def test_nvfp4_empty_single_and_poisoned_scales():
     assert st == 0 and np.isfinite(ref).all()
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert_attention_close(out, ref, "nvfp4 edge cases")
+    assert_attention_close(out, ref, "nvfp4 edge cases", twin=fp32_twin(s))
     assert (out[0] == 0).all()
 
 
@@ -666,7 +707,7 @@ def test_tc_q_far_outside_fp16_range(name):
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, f"{name} q x 2^20")
+    assert_attention_close(out, ref, f"{name} q x 2^20", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("name", QUANTISED)
@@ -681,7 +722,7 @@ def test_tc_sharp_softmax_rescales(name, boost):
     assert st == 0
     out, err = gpu_step(s)
     assert err == 0
-    assert_attention_close(out, ref, f"{name} scale x {boost}")
+    assert_attention_close(out, ref, f"{name} scale x {boost}", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("kv", ["fp8", "nvfp4", "bf16"])
@@ -700,7 +741,7 @@ def test_tc_groups_with_ragged_tails(kv, H, H_kv):
     assert st == 0 and np.isfinite(ref).all()
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert_attention_close(out, ref, f"{kv} H={H} H_kv={H_kv} ragged")
+    assert_attention_close(out, ref, f"{kv} H={H} H_kv={H_kv} ragged", twin=fp32_twin(s))
 
 
 # ------------------------------------------------------------------ quantised edge cases
@@ -714,7 +755,7 @@ def test_quantised_sm_cap_does_not_change_results(name, cap):
     ref, _, _, _ = oracle_full_step(s, append=False)
     out, err = gpu_step(s, append=False, sm_cap=cap)
     assert err == 0
-    assert_attention_close(out, ref, f"{name} sm_cap={cap}")
+    assert_attention_close(out, ref, f"{name} sm_cap={cap}", twin=fp32_twin(s, cap))
 
 
 @pytest.mark.parametrize("name", ["gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4"])
@@ -746,7 +787,7 @@ def test_quantised_single_very_long_request_split_over_every_worker(name):
     assert st == 0
     out, err = gpu_step(s, append=False)
     assert err == 0
-    assert_attention_close(out, ref, f"{name} one long request")
+    assert_attention_close(out, ref, f"{name} one long request", twin=fp32_twin(s))
 
 
 # ------------------------------------------------------------------ physical block sizes
@@ -781,7 +822,7 @@ def test_block_sizes_full_step(name, kw, bs):
     assert np.array_equal(to_np(s.v_cache).view(np.uint8), vc.view(np.uint8))
     if ksc is not None:
         assert np.array_equal(to_np(s.k_bscales), ksc) and np.array_equal(to_np(s.v_bscales), vsc)
-    assert_attention_close(out, ref, f"{name} {kw} block_size={bs}")
+    assert_attention_close(out, ref, f"{name} {kw} block_size={bs}", twin=fp32_twin(s))
 
 
 @pytest.mark.parametrize("bs", [32, 64])
@@ -794,7 +835,8 @@ def test_block_sizes_pack_unpack_and_caps(bs):
     for cap in (3, 61, 0):
         out, err = gpu_step(s, append=False, sm_cap=cap)
         assert err == 0
-        assert_attention_close(out, ref, f"block_size={bs} sm_cap={cap}")
+        assert_attention_close(out, ref, f"block_size={bs} sm_cap={cap}",
+                               twin=fp32_twin(s, cap))
     kc, vc = to_np(s.k_cache).copy(), to_np(s.v_cache).copy()
     r = int(np.argmax(s.context_lens_np))
     L = int(s.context_lens_np[r])

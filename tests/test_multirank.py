@@ -61,3 +61,14 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_flag_must_match_the_launched_ranks():
+    """--gpus N without N launched processes is refused (it would run one replica and
+    report one GPU)."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--config", "tiny", "--steps", "1"],
+                       capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert r.returncode == 2
+    assert "nproc-per-node 2" in r.stderr and not r.stdout.strip()
