@@ -36,6 +36,7 @@
 //    2 G query heads.
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 #include <type_traits>
 #include <cmath>
@@ -106,7 +107,9 @@ struct AttnParams {
   float* ws_o;                    // [2 * num_workers][G][D]   piece outputs
   float* ws_ml;                   // [2 * num_workers][G][2]   piece (max, sum)
   unsigned long long* ws_arrive;  // [B * H_kv] piece arrivals: call number << 16 | count
+  unsigned long long* ws_claim;   // pool chunks claimed so far: call number << 16 | count
   unsigned long long call;        // this call's number (48 bits)
+  int pool_k;                     // most pool chunks per warp the workspace holds pieces for
   int32_t* error_word;
   float v_scale;                  // value of a stored V element = code * v_scale (1 if plain)
   const uint8_t* k_bscales;       // NVFP4: [blocks, H_kv, 16, D/16] E4M3 block scales
@@ -122,13 +125,84 @@ struct AttnParams {
   uint32_t prefix_bytes;  // shared bytes reserved for the prefix table
 };
 
-// Worker w owns tiles [tile_start(w), tile_start(w + 1)).
-__host__ __device__ __forceinline__ int tile_start(int w, int W, int NW) {
-  return static_cast<int>((static_cast<long long>(w) * W) / NW);
-}
-// The worker whose range holds tile t (the largest w with tile_start(w) <= t).
-__host__ __device__ __forceinline__ int tile_owner(int t, int W, int NW) {
-  return static_cast<int>(((static_cast<long long>(t) + 1) * NW - 1) / W);
+#ifndef PDA_POOL_PCT
+#define PDA_POOL_PCT 10          // share of each warp's range left to claimed chunks
+#endif
+#ifndef PDA_POOL_CHUNKS_PER_WARP
+#define PDA_POOL_CHUNKS_PER_WARP 2  // chunks each warp's pooled share is cut into (at most)
+#endif
+constexpr int kMinChunkTiles = 4;  // a pool chunk is at least about this many tiles
+
+// Work units over the tile list. Warp w's range [a_w, a_{w+1}) (an equal split of the W
+// tiles over the NW warps) is cut into its static share [a_w, m_w), which warp w runs
+// itself, and k chunks of the remaining PDA_POOL_PCT percent, which any warp may claim once
+// its own static share is done. SMs stream at different rates (whole groups of them
+// consistently slower than the rest), and an equal static split ends with the slowest; the
+// claimed chunks move the last tenth of the work to the SMs that are ahead. Keeping each
+// chunk beside its warp's static share cuts a long (request, kv-head) segment into a few
+// pieces more, not into hundreds as a pool at the end of the list would. Units are numbered
+// in tile order (u = w (k + 1) + j: j = 0 the static share, j = 1..k the chunks), so the
+// pieces of a segment are merged in the same order whichever warp ran each chunk, and
+// results do not depend on timing. With k = 0 the units are the plain equal split.
+struct Units {
+  int W, NW, k;
+  int q, r;       // W = q NW + r
+  float per_inv;  // NW / W, for a first guess of a tile's warp
+  // a(w): first tile of warp w's range, floor(w W / NW) (w r < NW^2 < 2^32)
+  __host__ __device__ __forceinline__ int a(int w) const {
+    return w * q + static_cast<int>((static_cast<unsigned>(w) * static_cast<unsigned>(r)) /
+                                    static_cast<unsigned>(NW));
+  }
+  // m_w: end of warp w's static share
+  __host__ __device__ __forceinline__ static int m_of(int aw, int aw1) {
+    return aw + static_cast<int>((static_cast<long long>(aw1 - aw) * (100 - PDA_POOL_PCT)) / 100);
+  }
+  __host__ __device__ __forceinline__ int units() const { return NW * (k + 1); }
+  __host__ __device__ __forceinline__ int start(int u) const {
+    if (k == 0) return a(u);
+    const int w = k == 1 ? (u >> 1) : u / 3, j = u - w * (k + 1);
+    const int aw = a(w);
+    if (j == 0) return aw;
+    const int aw1 = a(w + 1), mw = m_of(aw, aw1);
+    return j == 1 ? mw : mw + ((aw1 - mw) >> 1);
+  }
+  // the warp whose range holds tile t: the largest w with a(w) <= t
+  __host__ __device__ __forceinline__ int warp_of(int t) const {
+    int w = static_cast<int>(static_cast<float>(t) * per_inv);
+    w = w < 0 ? 0 : (w >= NW ? NW - 1 : w);
+    while (w + 1 < NW && a(w + 1) <= t) ++w;
+    while (w > 0 && a(w) > t) --w;
+    return w;
+  }
+  // the unit whose range holds tile t
+  __host__ __device__ __forceinline__ int owner(int t) const {
+    const int w = warp_of(t);
+    if (k == 0) return w;
+    const int aw1 = a(w + 1), mw = m_of(a(w), aw1);
+    if (t < mw) return w * (k + 1);
+    if (k == 1) return 2 * w + 1;
+    return 3 * w + (t < mw + ((aw1 - mw) >> 1) ? 1 : 2);
+  }
+  __host__ __device__ __forceinline__ bool live(int u) const { return start(u) != start(u + 1); }
+  // Pool chunk g (claim order) -> its unit: first chunk 1 of every warp, then chunk 2, ...
+  __host__ __device__ __forceinline__ int chunk_unit(int g) const {
+    return (g % NW) * (k + 1) + 1 + g / NW;
+  }
+};
+static_assert(PDA_POOL_CHUNKS_PER_WARP >= 0 && PDA_POOL_CHUNKS_PER_WARP <= 2,
+              "Units cuts a warp's pooled share into at most two chunks");
+
+// The units of W tiles over NW warps, with at most k_max chunks per warp (0: all static).
+// Chunks stay at least kMinChunkTiles tiles, so short launches keep the plain split.
+__host__ __device__ __forceinline__ Units make_units(int W, int NW, int k_max) {
+  int k = 0;  // stays a compile-time 0 where k_max is one (the tensor-core steps)
+  if (k_max > 0) {
+    const long long kc = (static_cast<long long>(W) * PDA_POOL_PCT) /
+                         (100ll * NW * kMinChunkTiles);
+    k = kc < k_max ? static_cast<int>(kc) : k_max;
+  }
+  return Units{W, NW, k, W / NW, W % NW,
+               W > 0 ? static_cast<float>(NW) / static_cast<float>(W) : 0.f};
 }
 
 // Reduce-scatter over the lanes of one row group: n values per lane, xor masks from
@@ -476,29 +550,44 @@ __device__ __forceinline__ unsigned arrive(unsigned long long* counter,
   }
 }
 
+// Makes the pool's claim counter this call's, with nothing claimed yet, unless it already is
+// (a counter of another call, or one never written, is replaced). Each warp does this once,
+// before its first claim.
+__device__ __forceinline__ void register_claims(unsigned long long* c, unsigned long long call) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
+  while (((old ^ kTagMix) >> 16) != call) {
+    const unsigned long long seen = atomicCAS(c, old, arrival_reset(call));
+    if (seen == old) return;
+    old = seen;
+  }
+}
+
+// Claims the next pool chunk and returns its index (NW k or more once the pool is used up).
+// The tag mix leaves the low 16 bits alone, so the count adds without unmixing; a call makes
+// at most NW k + NW claims, below 2^16.
+__device__ __forceinline__ unsigned claim_chunk(unsigned long long* c) {
+  return static_cast<unsigned>(atomicAdd(c, 1ull) & 0xffffull);
+}
+
 // Log-sum-exp merge of the pieces of one segment (request b, kv-head h) into out, done by
-// the warp that registered the segment's last piece. Pieces come from workers w0..w1 (the
-// first may hold it as its tail piece); empty workers hold none. For each head j:
+// the warp that registered the segment's last piece. Pieces come from units w0..w1 (the
+// first may hold it as its tail piece); empty units hold none. For each head j:
 //   M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum o_i 2^(m_i - M) / L.
 // All heads are merged together so the loads of one pass are in flight at once: lane i
 // reads piece i's (m, l) of every head, then lanes stream the pieces' o rows. Pieces are
 // read from L2 (ld.cg): other SMs wrote them during this launch.
 template <int D, int G, int HP>
 __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, int j0, int w0,
-                                            int w1, bool w0_tail, int W_tiles, int NW,
-                                            int lane) {
+                                            int w1, bool w0_tail, const Units un, int lane) {
   constexpr int PER = D / 32;
   auto slot_of = [&](int w) { return 2 * w + ((w == w0 && w0_tail) ? 1 : 0); };
-  auto live = [&](int w) {
-    return tile_start(w, W_tiles, NW) != tile_start(w + 1, W_tiles, NW);
-  };
   const float* ml = p.ws_ml;
-  // pass 1: M[j] over all pieces
+  // pass 1: M[j] over all pieces (lane i looks at unit w0 + i, w0 + i + 32, ...)
   float M[HP];
 #pragma unroll
   for (int j = 0; j < HP; ++j) M[j] = -INFINITY;
   for (int w = w0 + lane; w <= w1; w += 32) {
-    if (!live(w)) continue;
+    if (!un.live(w)) continue;
     const float2* mlw =
         reinterpret_cast<const float2*>(ml) + static_cast<size_t>(slot_of(w)) * G + j0;
 #pragma unroll
@@ -522,7 +611,9 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
     float f[HP];
 #pragma unroll
     for (int j = 0; j < HP; ++j) f[j] = 0.f;
-    if (w <= w1 && live(w)) {
+    const bool mine = w <= w1 && un.live(w);
+    const unsigned live_mask = __ballot_sync(kFullMask, mine);  // bit i: unit base + i
+    if (mine) {
       const float2* mlw =
           reinterpret_cast<const float2*>(ml) + static_cast<size_t>(slot_of(w)) * G + j0;
 #pragma unroll
@@ -544,7 +635,7 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u;
-        use[u] = i < n && live(base + i);
+        use[u] = i < n && ((live_mask >> i) & 1u);
         const float* row =
             p.ws_o + (static_cast<size_t>(slot_of(use[u] ? base + i : w0)) * G + j0) * D;
 #pragma unroll
@@ -580,11 +671,11 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
 // Merges all G heads of a segment, at most four heads per pass (register budget).
 template <int D, int G>
 __device__ void merge_segment(const AttnParams& p, int b, int h, int w0, int w1, bool w0_tail,
-                              int W_tiles, int NW, int lane) {
+                              const Units un, int lane) {
   constexpr int HP = G < 4 ? G : 4;
 #pragma unroll 1
   for (int j0 = 0; j0 < G; j0 += HP)
-    merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, W_tiles, NW, lane);
+    merge_heads<D, G, HP>(p, b, h, j0, w0, w1, w0_tail, un, lane);
 }
 
 // MODE selects the tile step: kModeCuda (CUDA cores), kModeTc (tensor cores, one kv-head
@@ -684,14 +775,14 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
     }
   }
 
-  // ---- 3. this warp's tile range
+  // ---- 3. this warp's work: its static unit, then pool chunks while any are left
   const int H_kv = p.H_kv;
   const int W_tiles = s_pre[B] * H_kv;
-  const int NW = p.num_workers;
-  const int w = blockIdx.x * nwarps + warp;
-  const int t_begin = tile_start(w, W_tiles, NW);
-  const int t_end = tile_start(w + 1, W_tiles, NW);
-  if (t_begin >= t_end) return;
+  // Only the CUDA-core step leaves a pool (see make_plan); the tensor-core steps compile
+  // without it.
+  const Units un = make_units(W_tiles, p.num_workers, MODE == kModeCuda ? p.pool_k : 0);
+  const int w = (blockIdx.x * nwarps + warp) * (un.k + 1);  // this warp's static unit
+  if (un.k == 0 && !un.live(w)) return;
 
   unsigned char* my_stage = s_stage + static_cast<size_t>(warp) * p.stages * p.stage_bytes;
   uint64_t* my_bar = s_bar + warp * p.stages;
@@ -729,204 +820,246 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
     prefetch_tensormap(&tmV);
   }
   const uint64_t policy = l2_policy_evict_first();
-
-  // Issue-side metadata, one group of 32 tiles at a time: lane i describes tile
-  // g_base + i. The block id and context length of the next group are fetched with
-  // cp.async a whole group ahead into this warp's two-slot ring, so the lane that issues a
-  // tile never waits on a global load. Each lane reads only the slot it filled itself.
   int2* my_meta = s_meta + warp * 64;
-  int g_base = t_begin, g_buf = 0;
-  int cur_b = 0, cur_h = 0, cur_blk = 0, cur_pid = 0, cur_len = 0;
-  int nxt_b = 0, nxt_h = 0, nxt_blk = 0;
-  auto prefetch = [&](int base, int buf) {
-    const int y = base + lane;
-    if (y < t_end) {
-      int nb;
-      locate(y, nxt_b, nxt_h, nxt_blk, nb);
-      cp_async4(&my_meta[buf * 32 + lane].x, p.block_tables +
-                                                     static_cast<size_t>(nxt_b) * p.max_blocks +
-                                                     (nxt_blk >> p.bs_shift));
-      cp_async4(&my_meta[buf * 32 + lane].y, p.context_lens + nxt_b);
-    }
-    cp_async_commit();
-  };
-  auto enter = [&](int base, int buf) {  // the group starting at `base` becomes current
-    cp_async_wait_all();
-    g_base = base;
-    g_buf = buf;
-    cur_b = nxt_b;
-    cur_h = nxt_h;
-    cur_blk = nxt_blk;
-    const int2 m = my_meta[buf * 32 + lane];
-    cur_pid = m.x;
-    cur_len = m.y;
-    if (base + 32 < t_end) prefetch(base + 32, buf ^ 1);
-  };
-  prefetch(t_begin, 0);
-  enter(t_begin, 0);
-  auto issue = [&](int x, int s) {
-    if (x >= g_base + 32) enter(g_base + 32, g_buf ^ 1);
-    if (lane == x - g_base) {
-      const bool bad = cur_pid < 0 || cur_pid >= p.num_blocks;
-      const bool need_q = (cur_blk == 0) || (x == t_begin);
-      const int n_valid = min(kBS, cur_len - cur_blk * kBS);
-      my_info[s] = n_valid | (bad ? 0x100 : 0);
-      if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
-      const uint32_t bytes = 2 * kTile + 2 * kScales + (need_q ? Geo::Q_BYTES : 0);
-      mbar_arrive_expect_tx(&my_bar[s], bytes);
-      // the tile is rows sub * 16 .. + 15 of its physical block
-      const int sub = cur_blk & ((1 << p.bs_shift) - 1);
-      const int row = (bad ? 0 : cur_pid) * p.block_size + sub * kBS;
-      if constexpr (Geo::SCALED) {
-        // scales [blocks][heads][block_size][D/16]: each head's 16 rows are one run; with
-        // 16-token blocks a pair's two runs are adjacent (one copy)
-        constexpr uint32_t kRun = Geo::SCALE_BYTES;  // one head's 16 rows
-        const size_t head0 = static_cast<size_t>(bad ? 0 : cur_pid) * H_kv * kHeads +
-                             static_cast<size_t>(cur_h) * kHeads;
-        const size_t off = (head0 * p.block_size + static_cast<size_t>(sub) * kBS) *
-                           Geo::ROW_SCALES;
-        if (kHeads == 1 || p.bs_shift == 0) {
-          bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
-          bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
-        } else {
-          const size_t step = static_cast<size_t>(p.block_size) * Geo::ROW_SCALES;
-#pragma unroll
-          for (int u = 0; u < kHeads; ++u) {
-            bulk_load(ks_buf(s) + u * kRun, p.k_bscales + off + u * step, kRun, &my_bar[s]);
-            bulk_load(vs_buf(s) + u * kRun, p.v_bscales + off + u * step, kRun, &my_bar[s]);
-          }
-        }
-      }
-      if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
-        tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
-        tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);
-      } else {
-        tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
-        tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
-      }
-      if (need_q) {
-        const QT* src = reinterpret_cast<const QT*>(p.q) +
-                        (static_cast<size_t>(cur_b) * p.H + static_cast<size_t>(cur_h) * G) * D;
-        bulk_load(q_buf(s), src, Geo::Q_BYTES, &my_bar[s]);
-      }
-    }
-  };
-
   const int S = p.stages;
-  const int n_tiles = t_end - t_begin;
-  for (int i = 0; i < S && i < n_tiles; ++i) issue(t_begin + i, i);
-
-  // Consumer-side sequential position.
-  int cb, ch, cblk, cnb;
-  locate(t_begin, cb, ch, cblk, cnb);
-  W st;
-  st.init(lane);
-  bool seg_bad = false;
+  // The stage ring persists across units: every tile a unit loads is consumed within it, so
+  // the next unit starts on the stage (and phase) after the last one used.
   int stage = 0;
   uint32_t phase = 0;
+  W st;
+  st.init(lane);
+  bool registered = false;
 
-  for (int x = t_begin; x < t_end; ++x) {
-    const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&my_bar[stage], phase));
-    if (!ready) {
-      atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
-      cp_async_wait_all();
-      // Give copies still in flight a bounded chance to land before leaving.
-      for (int y = x; y < min(t_end, x + S); ++y) {
-        const int s2 = (stage + (y - x)) % S;
-        const uint32_t ph2 = phase ^ (((stage + (y - x)) / S) & 1);
-        mbar_wait_bounded(&my_bar[s2], ph2);
+  // Runs tiles [t_begin, t_end) as unit `unit`. When claim_next is set, lane 0 claims the
+  // next pool chunk as soon as the range has no more tiles to load (the atomic's latency
+  // hides behind the range's last tiles); the claimed index is returned through `claimed`.
+  // Returns false after a wait that timed out (the error bit is set).
+  auto run = [&](int t_begin, int t_end, int unit, bool claim_next, unsigned& claimed) -> bool {
+    // Issue-side metadata, one group of 32 tiles at a time: lane i describes tile
+    // g_base + i. The block id and context length of the next group are fetched with
+    // cp.async a whole group ahead into this warp's two-slot ring, so the lane that issues a
+    // tile never waits on a global load. Each lane reads only the slot it filled itself.
+    int g_base = t_begin, g_buf = 0;
+    int cur_b = 0, cur_h = 0, cur_blk = 0, cur_pid = 0, cur_len = 0;
+    int nxt_b = 0, nxt_h = 0, nxt_blk = 0;
+    auto prefetch = [&](int base, int buf) {
+      const int y = base + lane;
+      if (y < t_end) {
+        int nb;
+        locate(y, nxt_b, nxt_h, nxt_blk, nb);
+        cp_async4(&my_meta[buf * 32 + lane].x, p.block_tables +
+                                                       static_cast<size_t>(nxt_b) * p.max_blocks +
+                                                       (nxt_blk >> p.bs_shift));
+        cp_async4(&my_meta[buf * 32 + lane].y, p.context_lens + nxt_b);
       }
-      return;
-    }
-    const int info = my_info[stage];
-    const int n_valid = info & 0xff;
-    if (cblk == 0 || x == t_begin) {
-      st.reset(q_buf(stage), p.scale_log2);
-      seg_bad = false;
-    }
-    seg_bad |= (info & 0x100) != 0;
-    if (n_valid == kBS)
-      st.template tile<false>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
-                              n_valid);
-    else
-      st.template tile<true>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
-                             n_valid);
-
-    // hand the stage back to the TMA engine
-    __syncwarp();
-    fence_proxy_async_smem();
-    if (x + S < t_end) issue(x + S, stage);
-    if (++stage == S) {
-      stage = 0;
-      phase ^= 1;
-    }
-
-    // segment end?
-    const bool last_of_seg = (cblk + 1 == cnb);
-    if (last_of_seg || x + 1 == t_end) {
-      float lj[G], mj[G];
-      st.reduce(lj, mj);
-      const int seg_start = s_pre[cb] * H_kv + ch * cnb;
-      const int seg_end = seg_start + cnb;
-      const bool complete = seg_start >= t_begin && seg_end <= t_end;
-      if (complete) {
-        st.for_each_out(lj, [&](int j, int d, const float* o, int n, float l) {
-          float v[8];
-          const float inv = seg_bad ? __int_as_float(0x7fc00000) : p.v_scale / l;
+      cp_async_commit();
+    };
+    auto enter = [&](int base, int buf) {  // the group starting at `base` becomes current
+      cp_async_wait_all();
+      g_base = base;
+      g_buf = buf;
+      cur_b = nxt_b;
+      cur_h = nxt_h;
+      cur_blk = nxt_blk;
+      const int2 m = my_meta[buf * 32 + lane];
+      cur_pid = m.x;
+      cur_len = m.y;
+      if (base + 32 < t_end) prefetch(base + 32, buf ^ 1);
+    };
+    prefetch(t_begin, 0);
+    enter(t_begin, 0);
+    auto issue = [&](int x, int s) {
+      if (x >= g_base + 32) enter(g_base + 32, g_buf ^ 1);
+      if (lane == x - g_base) {
+        const bool bad = cur_pid < 0 || cur_pid >= p.num_blocks;
+        const bool need_q = (cur_blk == 0) || (x == t_begin);
+        const int n_valid = min(kBS, cur_len - cur_blk * kBS);
+        my_info[s] = n_valid | (bad ? 0x100 : 0);
+        if (bad) atomic_or_error(p.error_word, PDA_DEVERR_BLOCK_ID);
+        const uint32_t bytes = 2 * kTile + 2 * kScales + (need_q ? Geo::Q_BYTES : 0);
+        mbar_arrive_expect_tx(&my_bar[s], bytes);
+        // the tile is rows sub * 16 .. + 15 of its physical block
+        const int sub = cur_blk & ((1 << p.bs_shift) - 1);
+        const int row = (bad ? 0 : cur_pid) * p.block_size + sub * kBS;
+        if constexpr (Geo::SCALED) {
+          // scales [blocks][heads][block_size][D/16]: each head's 16 rows are one run; with
+          // 16-token blocks a pair's two runs are adjacent (one copy)
+          constexpr uint32_t kRun = Geo::SCALE_BYTES;  // one head's 16 rows
+          const size_t head0 = static_cast<size_t>(bad ? 0 : cur_pid) * H_kv * kHeads +
+                               static_cast<size_t>(cur_h) * kHeads;
+          const size_t off = (head0 * p.block_size + static_cast<size_t>(sub) * kBS) *
+                             Geo::ROW_SCALES;
+          if (kHeads == 1 || p.bs_shift == 0) {
+            bulk_load(ks_buf(s), p.k_bscales + off, kScales, &my_bar[s]);
+            bulk_load(vs_buf(s), p.v_bscales + off, kScales, &my_bar[s]);
+          } else {
+            const size_t step = static_cast<size_t>(p.block_size) * Geo::ROW_SCALES;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (e < n) v[e] = o[e] * inv;
-          const size_t off =
-              (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D + d;
-          store_out(p.out, off, v, n, p.out_kind);
-        });
-      } else {
-        // A piece of a segment cut by a range boundary: store (m, l, o), register it, and
-        // merge the segment if this was its last piece.
-        const int slot = 2 * w + (seg_start <= t_begin ? 0 : 1);
-        st.for_each_out(lj, [&](int j, int d, const float* o, int n, float) {
-          store_f32(p.ws_o + (static_cast<size_t>(slot) * G + j) * D + d, o, n);
-        });
-        if (st.writes_ml(lane)) {
-#pragma unroll
-          for (int j = 0; j < G; ++j) {
-            p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
-            p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
-                seg_bad ? __int_as_float(0x7fc00000) : lj[j];
+            for (int u = 0; u < kHeads; ++u) {
+              bulk_load(ks_buf(s) + u * kRun, p.k_bscales + off + u * step, kRun, &my_bar[s]);
+              bulk_load(vs_buf(s) + u * kRun, p.v_bscales + off + u * step, kRun, &my_bar[s]);
+            }
           }
         }
-        __threadfence();  // this lane's piece stores before the arrival below
-        __syncwarp();
-        const int seg = cb * H_kv + ch;
-        unsigned arrived = 0;
-        if (lane == 0) arrived = arrive(p.ws_arrive + seg, p.call);
-        arrived = __shfl_sync(kFullMask, arrived, 0);
-        const int w0 = tile_owner(seg_start, W_tiles, NW);
-        const int w1 = tile_owner(seg_end - 1, W_tiles, NW);
-        unsigned pieces = 0;
-        for (int wb = w0; wb <= w1; wb += 32) {
-          const int ww = wb + lane;
-          const bool has = ww <= w1 && tile_start(ww, W_tiles, NW) != tile_start(ww + 1, W_tiles, NW);
-          pieces += __popc(__ballot_sync(kFullMask, has));
+        if constexpr (MODE == kModeTcPair) {  // both heads of pair cur_h in one box
+          tma_load_4d(k_buf(s), &tmK, 0, row, 0, cur_h, &my_bar[s], policy);
+          tma_load_4d(v_buf(s), &tmV, 0, row, 0, cur_h, &my_bar[s], policy);
+        } else {
+          tma_load_3d(k_buf(s), &tmK, 0, cur_h, row, &my_bar[s], policy);
+          tma_load_3d(v_buf(s), &tmV, 0, cur_h, row, &my_bar[s], policy);
         }
-        if (arrived == pieces) {
-          __threadfence();  // see the other pieces' stores
-          merge_segment<D, G>(p, cb, ch, w0, w1, seg_start != tile_start(w0, W_tiles, NW),
-                              W_tiles, NW, lane);
-          if (lane == 0) atomicExch(p.ws_arrive + seg, arrival_reset(p.call));
+        if (need_q) {
+          const QT* src = reinterpret_cast<const QT*>(p.q) +
+                          (static_cast<size_t>(cur_b) * p.H + static_cast<size_t>(cur_h) * G) * D;
+          bulk_load(q_buf(s), src, Geo::Q_BYTES, &my_bar[s]);
         }
+      }
+    };
+
+    const int n_tiles = t_end - t_begin;
+    for (int i = 0; i < S && i < n_tiles; ++i) issue(t_begin + i, (stage + i) % S);
+    if (claim_next && !registered) {  // overlaps the first loads
+      if (lane == 0) register_claims(p.ws_claim, p.call);
+      registered = true;
+    }
+    unsigned next_claim = 0;
+    if (claim_next && n_tiles < S && lane == 0) next_claim = claim_chunk(p.ws_claim);
+
+    // Consumer-side sequential position.
+    int cb, ch, cblk, cnb;
+    locate(t_begin, cb, ch, cblk, cnb);
+    bool seg_bad = false;
+
+    for (int x = t_begin; x < t_end; ++x) {
+      const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&my_bar[stage], phase));
+      if (!ready) {
+        atomic_or_error(p.error_word, PDA_DEVERR_TIMEOUT);
+        cp_async_wait_all();
+        // Give copies still in flight a bounded chance to land before leaving.
+        for (int y = x; y < min(t_end, x + S); ++y) {
+          const int s2 = (stage + (y - x)) % S;
+          const uint32_t ph2 = phase ^ (((stage + (y - x)) / S) & 1);
+          mbar_wait_bounded(&my_bar[s2], ph2);
+        }
+        return false;
+      }
+      const int info = my_info[stage];
+      const int n_valid = info & 0xff;
+      if (cblk == 0 || x == t_begin) {
+        st.reset(q_buf(stage), p.scale_log2);
+        seg_bad = false;
+      }
+      seg_bad |= (info & 0x100) != 0;
+      if (n_valid == kBS)
+        st.template tile<false>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
+                                n_valid);
+      else
+        st.template tile<true>(k_buf(stage), v_buf(stage), ks_buf(stage), vs_buf(stage),
+                               n_valid);
+
+      // hand the stage back to the TMA engine
+      __syncwarp();
+      fence_proxy_async_smem();
+      if (x + S < t_end)
+        issue(x + S, stage);
+      else if (claim_next && x + S == t_end && lane == 0)  // nothing left to load
+        next_claim = claim_chunk(p.ws_claim);
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1;
+      }
+
+      // segment end?
+      const bool last_of_seg = (cblk + 1 == cnb);
+      if (last_of_seg || x + 1 == t_end) {
+        float lj[G], mj[G];
+        st.reduce(lj, mj);
+        const int seg_start = s_pre[cb] * H_kv + ch * cnb;
+        const int seg_end = seg_start + cnb;
+        const bool complete = seg_start >= t_begin && seg_end <= t_end;
+        if (complete) {
+          st.for_each_out(lj, [&](int j, int d, const float* o, int n, float l) {
+            float v[8];
+            const float inv = seg_bad ? __int_as_float(0x7fc00000) : p.v_scale / l;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (e < n) v[e] = o[e] * inv;
+            const size_t off =
+                (static_cast<size_t>(cb) * p.H + static_cast<size_t>(ch) * G + j) * D + d;
+            store_out(p.out, off, v, n, p.out_kind);
+          });
+        } else {
+          // A piece of a segment cut by a unit boundary: store (m, l, o), register it, and
+          // merge the segment if this was its last piece.
+          const int slot = 2 * unit + (seg_start <= t_begin ? 0 : 1);
+          st.for_each_out(lj, [&](int j, int d, const float* o, int n, float) {
+            store_f32(p.ws_o + (static_cast<size_t>(slot) * G + j) * D + d, o, n);
+          });
+          if (st.writes_ml(lane)) {
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 0] = mj[j];
+              p.ws_ml[(static_cast<size_t>(slot) * G + j) * 2 + 1] =
+                  seg_bad ? __int_as_float(0x7fc00000) : lj[j];
+            }
+          }
+          __threadfence();  // this lane's piece stores before the arrival below
+          __syncwarp();
+          const int seg = cb * H_kv + ch;
+          unsigned arrived = 0;
+          if (lane == 0) arrived = arrive(p.ws_arrive + seg, p.call);
+          arrived = __shfl_sync(kFullMask, arrived, 0);
+          const int w0 = un.owner(seg_start);
+          const int w1 = un.owner(seg_end - 1);
+          unsigned pieces = 0;
+          for (int wb = w0; wb <= w1; wb += 32) {
+            const int ww = wb + lane;
+            pieces += __popc(__ballot_sync(kFullMask, ww <= w1 && un.live(ww)));
+          }
+          if (arrived == pieces) {
+            __threadfence();  // see the other pieces' stores
+            merge_segment<D, G>(p, cb, ch, w0, w1, seg_start != un.start(w0), un, lane);
+            if (lane == 0) atomicExch(p.ws_arrive + seg, arrival_reset(p.call));
+          }
+        }
+      }
+      // advance the consumer position
+      if (++cblk == cnb) {
+        cblk = 0;
+        if (++ch == H_kv) {
+          ch = 0;
+          do {
+            ++cb;
+          } while (cb < B && s_pre[cb + 1] == s_pre[cb]);
+        }
+        if (cb < B) cnb = s_pre[cb + 1] - s_pre[cb];
       }
     }
-    // advance the consumer position
-    if (++cblk == cnb) {
-      cblk = 0;
-      if (++ch == H_kv) {
-        ch = 0;
-        do {
-          ++cb;
-        } while (cb < B && s_pre[cb + 1] == s_pre[cb]);
-      }
-      if (cb < B) cnb = s_pre[cb + 1] - s_pre[cb];
+    claimed = __shfl_sync(kFullMask, next_claim, 0);
+    return true;
+  };
+
+  const bool pool = un.k > 0;
+  const unsigned n_chunks = static_cast<unsigned>(un.NW) * un.k;
+  unsigned c = 0;
+  if (un.live(w)) {
+    if (!run(un.start(w), un.start(w + 1), w, pool, c)) return;
+  } else if (pool) {
+    if (lane == 0) {
+      register_claims(p.ws_claim, p.call);
+      c = claim_chunk(p.ws_claim);
+    }
+    registered = true;
+    c = __shfl_sync(kFullMask, c, 0);
+  }
+  // pool chunks, each the next one nobody has taken yet
+  while (pool && c < n_chunks) {
+    const int u = un.chunk_unit(static_cast<int>(c));
+    if (un.live(u)) {
+      if (!run(un.start(u), un.start(u + 1), u, true, c)) return;
+    } else {
+      if (lane == 0) c = claim_chunk(p.ws_claim);
+      c = __shfl_sync(kFullMask, c, 0);
     }
   }
 }
@@ -936,9 +1069,10 @@ namespace {
 
 struct LaunchPlan {
   int nwarps, stages, grid;
+  int pool_k;  // pool chunks per warp the workspace has piece slots for (0: all static)
   uint32_t stage_bytes, prefix_bytes;
   size_t smem_bytes;
-  size_t ws_arrive, ws_ml, ws_o, ws_total;  // byte offsets / total
+  size_t ws_arrive, ws_claim, ws_ml, ws_o, ws_total;  // byte offsets / total
 };
 
 // q is bf16 beside a quantised cache, otherwise of the cache's own type.
@@ -976,7 +1110,9 @@ uint32_t stage_bytes_for(pda_dtype kv, int D, const Tiling& t) {
       round_up(2 * tile + scales + q, stage_align(t.mode != kModeCuda)));
 }
 
-bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms,
+// pool: leave a share of the tiles to chunks claimed at run time (see Units); the
+// workspace then holds piece slots for them as well.
+bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_sms, bool pool,
                LaunchPlan* pl) {
   const Tiling t = tiling_for(kv, D, H_kv, G);
   const bool tc = t.mode != kModeCuda;
@@ -1009,10 +1145,23 @@ bool make_plan(int B, int H_kv, int G, int D, pda_dtype kv, int sm_cap, int num_
   if (sm_cap > 0 && sm_cap < grid) grid = sm_cap;
   pl->grid = grid;
   const size_t nw_total = static_cast<size_t>(grid) * pl->nwarps;
+  // Pool chunks pay off where the grid covers the whole chip: there SMs stream at unequal
+  // rates (measured: whole runs of SMs about 10 % slower than the rest, at every workload),
+  // while a capped grid leaves room around its SMs and runs evenly, so the chunks' extra
+  // pieces and pipeline refills would cost more than they balance. The tensor-core steps
+  // (quantised caches) process a tile in a fraction of the time and pay relatively more for
+  // both; they keep the static split. A call claims at most NW k chunks plus one failed claim
+  // per warp, within 16 bits.
+  pl->pool_k = pool && t.mode == kModeCuda && grid == num_sms &&
+                       nw_total * (PDA_POOL_CHUNKS_PER_WARP + 1) < 65536
+                   ? PDA_POOL_CHUNKS_PER_WARP
+                   : 0;
+  const size_t units = nw_total * (1 + pl->pool_k);
   pl->ws_arrive = 0;
-  pl->ws_ml = round_up(static_cast<size_t>(B) * t.H_u * 8, 256);
-  pl->ws_o = pl->ws_ml + round_up(2 * nw_total * t.G_u * 2 * 4, 256);
-  pl->ws_total = pl->ws_o + round_up(2 * nw_total * t.G_u * static_cast<size_t>(D) * 4, 256);
+  pl->ws_claim = static_cast<size_t>(B) * t.H_u * 8;
+  pl->ws_ml = round_up(pl->ws_claim + 8, 256);
+  pl->ws_o = pl->ws_ml + round_up(2 * units * t.G_u * 2 * 4, 256);
+  pl->ws_total = pl->ws_o + round_up(2 * units * t.G_u * static_cast<size_t>(D) * 4, 256);
   return true;
 }
 
@@ -1160,7 +1309,8 @@ extern "C" pda_status pda_attention_workspace_size(int B, int H, int H_kv, int D
   const pda_status st = current_device_sms(&dev, &sms);
   if (st != PDA_OK) return st;
   LaunchPlan pl;
-  if (!make_plan(B, H_kv, H / H_kv, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  if (!make_plan(B, H_kv, H / H_kv, D, kv_dtype, sm_cap, sms, true, &pl))
+    return PDA_ERR_UNSUPPORTED;
   *bytes = pl.ws_total;
   return PDA_OK;
 }
@@ -1178,7 +1328,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
                             float k_scale, float v_scale, pda_dtype q_dtype,
                             pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
                             void* workspace, size_t workspace_bytes, int32_t* error_word,
-                            cudaStream_t stream, bool clear_arrivals = false) {
+                            cudaStream_t stream, bool pool = true, bool clear_arrivals = false) {
   // ---- host-side validation, before any CUDA call
   if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || sm_cap < 0 ||
@@ -1211,7 +1361,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   pda_status st = current_device_sms(&dev, &sms);
   if (st != PDA_OK) return st;
   LaunchPlan pl;
-  if (!make_plan(B, H_kv, G, D, kv_dtype, sm_cap, sms, &pl)) return PDA_ERR_UNSUPPORTED;
+  if (!make_plan(B, H_kv, G, D, kv_dtype, sm_cap, sms, pool, &pl)) return PDA_ERR_UNSUPPORTED;
   if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
 
   const Tiling tiling = tiling_for(kv_dtype, D, H_kv, G);
@@ -1241,6 +1391,8 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   ap.block_tables = block_tables;
   ap.context_lens = context_lens;
   ap.ws_arrive = reinterpret_cast<unsigned long long*>(ws + pl.ws_arrive);
+  ap.ws_claim = reinterpret_cast<unsigned long long*>(ws + pl.ws_claim);
+  ap.pool_k = pl.pool_k;
   ap.call = g_call.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1);
   ap.ws_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   ap.ws_o = reinterpret_cast<float*>(ws + pl.ws_o);
@@ -1267,9 +1419,7 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
 
   // clear_arrivals: zero the arrival counters first (a memset on the same stream), so no
   // counter left in the workspace by an earlier call can pass for one of this call's
-  if (clear_arrivals &&
-      cudaMemsetAsync(ap.ws_arrive, 0, static_cast<size_t>(B) * tiling.H_u * 8, stream) !=
-          cudaSuccess)
+  if (clear_arrivals && cudaMemsetAsync(ap.ws_arrive, 0, pl.ws_claim + 8, stream) != cudaSuccess)
     return PDA_ERR_CUDA;
   fn<<<pl.grid, pl.nwarps * 32, pl.smem_bytes, stream>>>(tmK, tmV, ap);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
@@ -1357,13 +1507,21 @@ extern "C" pda_status pda_paged_decode_attention_noalloc(
     float scale, pda_dtype q_dtype, pda_dtype kv_dtype, pda_dtype out_dtype, int sm_cap,
     int32_t* error_word, cudaStream_t stream) {
   if (kv_dtype == PDA_FP8_E4M3) return PDA_ERR_UNSUPPORTED;  // as pda_paged_decode_attention
-  size_t need = 0;
-  pda_status st = pda_attention_workspace_size(B, H, H_kv, D, block_size, kv_dtype, sm_cap,
-                                               &need);
+  // The same checks as pda_attention_workspace_size, for the all-static split (no pool of
+  // claimed chunks, whose piece slots would not fit the fixed array).
+  if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || D <= 0 || block_size <= 0 ||
+      sm_cap < 0 || !(dtype_ok(kv_dtype) || kv_dtype == PDA_NVFP4))
+    return PDA_ERR_INVALID_ARG;
+  if (!supported_block_size(block_size) || (D != 64 && D != 128) || !supported_g(H / H_kv) ||
+      B > kMaxBatch)
+    return PDA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  pda_status st = current_device_sms(&dev, &sms);
   if (st != PDA_OK) return st;
-  if (need > PDA_NOALLOC_SCRATCH_BYTES) return PDA_ERR_TOO_LARGE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  LaunchPlan pl;
+  if (!make_plan(B, H_kv, H / H_kv, D, kv_dtype, sm_cap, sms, false, &pl))
+    return PDA_ERR_UNSUPPORTED;
+  if (pl.ws_total > PDA_NOALLOC_SCRATCH_BYTES) return PDA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   st = noalloc_scratch(dev, &scratch);
   if (st != PDA_OK) return st;
@@ -1373,5 +1531,5 @@ extern "C" pda_status pda_paged_decode_attention_noalloc(
                           max_blocks_per_seq, context_lens, max_context_len, B, H, H_kv, D,
                           block_size, num_blocks, scale, 1.f, 1.f, q_dtype, kv_dtype, out_dtype,
                           sm_cap, scratch, PDA_NOALLOC_SCRATCH_BYTES, error_word, stream,
-                          /*clear_arrivals=*/true);
+                          /*pool=*/false, /*clear_arrivals=*/true);
 }

@@ -43,13 +43,17 @@ def lib():
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
-    """Calls of alternating shapes: each one's counters lie where the previous one left
-    partial results. The same kernel with the same plan runs behind both entry points, so
-    any difference at all would be scratch leaking between calls."""
+    """Calls of alternating shapes, each one's counters lying where the previous one left
+    partial results. Every output is held to the oracle (strict bound) and to the workspace
+    entry point within the same tolerance. The no-allocation call always splits the work
+    statically (the workspace call may leave a share to chunks claimed at run time, which
+    rounds differently in the last bits), so its own results must repeat bit for bit: a
+    repeat that differs would be scratch leaking from the call before."""
     steps = [wl.make_step("gqa_skew_b256", device="cuda", B=48),
              wl.make_step("llama2_13b_b80", device="cuda", B=20)]
     oracle = [oracle_full_step(s, append=False)[0] for s in steps]
-    for s, want in zip(steps + steps, oracle + oracle):
+    first = {}
+    for i, (s, want) in enumerate(zip(steps + steps, oracle + oracle)):
         ref = torch.empty_like(s.q)
         pda.paged_decode_attention(ref, s.q, s.k_cache, s.v_cache, s.block_tables,
                                    s.context_lens, s.max_context_len, s.scale)
@@ -59,8 +63,14 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
         torch.cuda.synchronize()
         assert st == binding.PDA_OK, binding.status_string(st)
         assert int(err.item()) == 0
-        assert torch.equal(out, ref), "noalloc differs from the workspace entry point"
         assert_attention_close(out, want, f"noalloc {s.w.name} vs oracle", strict=True)
+        assert_attention_close(out, ref.double().cpu().numpy(),
+                               f"noalloc {s.w.name} vs workspace entry point", strict=True)
+        key = i % len(steps)
+        if key in first:
+            assert torch.equal(out, first[key]), "a repeated call differs: scratch leaked"
+        else:
+            first[key] = out
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
