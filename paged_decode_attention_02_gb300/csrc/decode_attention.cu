@@ -722,6 +722,12 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   int2* s_meta = reinterpret_cast<int2*>(
       (reinterpret_cast<uintptr_t>(s_info + nwarps * p.stages) + 7) & ~uintptr_t(7));
 
+  // The tensor maps' descriptors are fetched while the prologue below reads the lengths.
+  if (tid == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+
   // ---- 1. block prefix sums of per-request tile counts (every block computes its own)
   const int cap_tokens = min(p.max_blocks * p.block_size, p.max_context_len);
   {
@@ -815,10 +821,6 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
     blk = rem - h * nb;
   };
 
-  if (lane == 0) {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
   const uint64_t policy = l2_policy_evict_first();
   int2* my_meta = s_meta + warp * 64;
   const int S = p.stages;
