@@ -45,6 +45,7 @@ NOMINAL_HBM_GBS = 8000.0  # GB300's HBM3e rate as the task names it (~8 TB/s)
 ATTN_SOURCES = ["paged_decode_attention_02_gb300/csrc/decode_attention.cu",
                 "paged_decode_attention_02_gb300/csrc/pda_device.cuh",
                 "paged_decode_attention_02_gb300/csrc/warp_attn_tc.cuh",
+                "paged_decode_attention_02_gb300/csrc/work_units.h",
                 "paged_decode_attention_02_gb300/csrc/pda_api.cu"]
 
 

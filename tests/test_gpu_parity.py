@@ -90,6 +90,21 @@ def test_full_size_sampled(name):
     assert torch.isfinite(out.float()).all()
 
 
+def test_full_size_pool_launches_are_bitwise_identical():
+    """At full size the headline workload leaves a tenth of each warp's range to chunks that
+    warps claim at run time (two per warp here: tiles x 10 % / (100 warps-per-tile-share x 4)
+    >= 2). Which warp runs which chunk changes from launch to launch; the pieces merge in
+    unit order, so repeated launches must agree bit for bit."""
+    s = wl.make_step("gqa_skew_b256", device=DEV)
+    tiles = int(((s.context_lens_np.astype(np.int64) + 15) // 16).sum()) * s.w.H_kv
+    warps = pda.device_sm_count() * 12
+    assert tiles * 10 // (100 * warps * 4) >= 2
+    a, err_a = gpu_step(s, append=False)
+    b, err_b = gpu_step(s, append=False)
+    assert err_a == 0 and err_b == 0
+    assert torch.equal(a, b)
+
+
 _FULL = {}
 
 
