@@ -58,6 +58,14 @@ namespace pda {
 #define PDA_ATTN_MAX_STAGES 4  // most pipeline stages per warp
 #endif
 
+// A launch uses no more warps than give each at least this many tiles. With fewer, a small
+// batch spreads over thousands of warps and every (request, kv-head) segment is cut into
+// dozens of pieces for its merge to read back: one 13B-shape request ran 51 us over 1824
+// warps and 31 us at 8 tiles per warp (4 and 16 measured slower).
+#ifndef PDA_MIN_TILES_PER_WARP
+#define PDA_MIN_TILES_PER_WARP 8
+#endif
+
 #ifndef PDA_TC_WARPS
 #define PDA_TC_WARPS 12        // warps (workers) per block of the tensor-core tile step
 #endif
@@ -544,24 +552,28 @@ __device__ __forceinline__ void merge_heads(const AttnParams& p, int b, int h, i
         Lsum[j] += v.y * f[j];
       }
     }
-    const int n = min(32, w1 - base + 1);
-    // U pieces' rows in flight at once (each load is an L2 round trip). A dead or missing
-    // piece reads piece w0's row (always written: w0 holds the segment's first tile) and is
-    // left out of the sum by its flag, not by a zero weight (its row may hold NaN).
+    // The live pieces of this group of 32 units, U rows in flight at once (each load is an L2
+    // round trip), in increasing unit order. Empty units are skipped outright: a launch with
+    // fewer tiles than warps leaves most units empty, and a segment's range of units can
+    // hold hundreds of them. A missing slot of the last batch reads piece w0's row (always
+    // written: w0 holds the segment's first tile) and is left out of the sum by its flag, not
+    // by a zero weight (its row may hold NaN).
     constexpr int U = HP * PER <= 4 ? 4 : 1;  // wider would spill in the kernels with G >= 2
-    for (int i0 = 0; i0 < n; i0 += U) {
+    unsigned rest = live_mask;  // the same on every lane
+    while (rest != 0u) {
       float v[U][HP][PER];
       float fu[U][HP];
       bool use[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int i = i0 + u;
-        use[u] = i < n && ((live_mask >> i) & 1u);
+        use[u] = rest != 0u;
+        const int i = use[u] ? __ffs(rest) - 1 : 0;
+        rest &= rest - 1u;  // no-op once empty
         const float* row =
             p.ws_o + (static_cast<size_t>(slot_of(use[u] ? base + i : w0)) * G + j0) * D;
 #pragma unroll
         for (int j = 0; j < HP; ++j) {
-          fu[u][j] = __shfl_sync(kFullMask, f[j], i < n ? i : 0);
+          fu[u][j] = __shfl_sync(kFullMask, f[j], i);
 #pragma unroll
           for (int e = 0; e < PER; ++e) v[u][j][e] = __ldcg(row + j * D + lane + 32 * e);
         }
@@ -707,8 +719,15 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   const int W_tiles = s_pre[B] * H_kv;
   // Only the CUDA-core step leaves a pool (see make_plan); the tensor-core steps compile
   // without it.
-  const Units un = make_units(W_tiles, p.num_workers, MODE == kModeCuda ? p.pool_k : 0);
-  const int w = (blockIdx.x * nwarps + warp) * (un.k + 1);  // this warp's static unit
+  // Workers: the grid's warps, but no more than give each PDA_MIN_TILES_PER_WARP tiles of
+  // this launch (the host sized the grid by its bound on the lengths; the lengths on the
+  // device may be shorter). The others leave here.
+  const int nw = max(1, min(p.num_workers,
+                            (W_tiles + PDA_MIN_TILES_PER_WARP - 1) / PDA_MIN_TILES_PER_WARP));
+  const int wi = blockIdx.x * nwarps + warp;
+  if (wi >= nw) return;
+  const Units un = make_units(W_tiles, nw, MODE == kModeCuda ? p.pool_k : 0);
+  const int w = wi * (un.k + 1);  // this warp's static unit
   if (un.k == 0 && !un.live(w)) return;
 
   unsigned char* my_stage = s_stage + static_cast<size_t>(warp) * p.stages * p.stage_bytes;
@@ -1288,6 +1307,21 @@ pda_status launch_attention(void* out, const void* q, const void* k_cache, const
   if (workspace_bytes < pl.ws_total) return PDA_ERR_WORKSPACE;
 
   const Tiling tiling = tiling_for(kv_dtype, D, H_kv, G);
+  // No more blocks than give every warp PDA_MIN_TILES_PER_WARP tiles at the host's bound on
+  // the lengths (every request at max_context_len); the kernel applies the same rule to the
+  // lengths it reads. The workspace, sized for the full grid, is large enough for fewer
+  // workers.
+  {
+    const long long max_len =
+        std::min<long long>(max_context_len, static_cast<long long>(max_blocks_per_seq) * block_size);
+    const long long tiles = static_cast<long long>(B) * tiling.H_u * ((max_len + kBS - 1) / kBS);
+    const long long per_block = static_cast<long long>(pl.nwarps) * PDA_MIN_TILES_PER_WARP;
+    const long long blocks = (tiles + per_block - 1) / per_block;
+    if (blocks < pl.grid) {
+      pl.grid = static_cast<int>(std::max<long long>(1, blocks));
+      pl.pool_k = 0;  // the pool is for the whole chip's grid
+    }
+  }
   KernelFn fn = pick_kernel(kv_dtype, D, tiling);
   if (fn == nullptr) return PDA_ERR_UNSUPPORTED;
   st = allow_max_smem(reinterpret_cast<const void*>(fn), dev);
