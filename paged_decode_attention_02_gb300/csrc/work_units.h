@@ -18,6 +18,9 @@ namespace pda {
 #ifndef PDA_POOL_CHUNKS_PER_WARP
 #define PDA_POOL_CHUNKS_PER_WARP 2  // chunks each warp's pooled share is cut into (at most)
 #endif
+#ifndef PDA_POOL_FIRST_CHUNK_PCT
+#define PDA_POOL_FIRST_CHUNK_PCT 50  // share of a warp's pooled tiles in its first chunk (k = 2)
+#endif
 constexpr int kMinChunkTiles = 4;  // a pool chunk is at least about this many tiles
 
 // Work units over the tile list. Warp w's range [a_w, a_{w+1}) (an equal split of the W
@@ -51,7 +54,12 @@ struct Units {
     const int aw = a(w);
     if (j == 0) return aw;
     const int aw1 = a(w + 1), mw = m_of(aw, aw1);
-    return j == 1 ? mw : mw + ((aw1 - mw) >> 1);
+    return j == 1 ? mw : mid(mw, aw1);
+  }
+  // end of the first chunk of a warp whose pooled tiles are [mw, aw1) (k = 2)
+  PDA_HD static int mid(int mw, int aw1) {
+    return mw + static_cast<int>((static_cast<long long>(aw1 - mw) * PDA_POOL_FIRST_CHUNK_PCT) /
+                                 100);
   }
   // the warp whose range holds tile t: the largest w with a(w) <= t
   PDA_HD int warp_of(int t) const {
@@ -68,7 +76,7 @@ struct Units {
     const int aw1 = a(w + 1), mw = m_of(a(w), aw1);
     if (t < mw) return w * (k + 1);
     if (k == 1) return 2 * w + 1;
-    return 3 * w + (t < mw + ((aw1 - mw) >> 1) ? 1 : 2);
+    return 3 * w + (t < mid(mw, aw1) ? 1 : 2);
   }
   PDA_HD bool live(int u) const { return start(u) != start(u + 1); }
   // Pool chunk g (claim order) -> its unit: first chunk 1 of every warp, then chunk 2, ...
