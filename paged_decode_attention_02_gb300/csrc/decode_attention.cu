@@ -113,10 +113,10 @@ struct AttnParams {
   const void* q;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* ws_o;                    // [2 * num_workers][G][D]   piece outputs
-  float* ws_ml;                   // [2 * num_workers][G][2]   piece (max, sum)
-  unsigned long long* ws_arrive;  // [B * H_kv] piece arrivals: call number << 16 | count
-  unsigned long long* ws_claim;   // pool chunks claimed so far: call number << 16 | count
+  float* ws_o;                    // [2 * units][G][D]   piece outputs (two slots per unit)
+  float* ws_ml;                   // [2 * units][G][2]   piece (max, sum)
+  unsigned long long* ws_arrive;  // [B * H_kv] piece arrivals (tagged counters, see arrive)
+  unsigned long long* ws_claim;   // pool chunks claimed so far (tagged counter)
   unsigned long long call;        // this call's number (48 bits)
   int pool_k;                     // most pool chunks per warp the workspace holds pieces for
   int32_t* error_word;
@@ -717,11 +717,10 @@ __global__ void __launch_bounds__(warps_for_mode(G, MODE, std::is_same<KV, nvfp4
   // ---- 3. this warp's work: its static unit, then pool chunks while any are left
   const int H_kv = p.H_kv;
   const int W_tiles = s_pre[B] * H_kv;
-  // Only the CUDA-core step leaves a pool (see make_plan); the tensor-core steps compile
-  // without it.
   // Workers: the grid's warps, but no more than give each PDA_MIN_TILES_PER_WARP tiles of
   // this launch (the host sized the grid by its bound on the lengths; the lengths on the
-  // device may be shorter). The others leave here.
+  // device may be shorter). The others leave here. Only the CUDA-core step leaves a pool
+  // (see make_plan); the tensor-core steps compile without it.
   const int nw = max(1, min(p.num_workers,
                             (W_tiles + PDA_MIN_TILES_PER_WARP - 1) / PDA_MIN_TILES_PER_WARP));
   const int wi = blockIdx.x * nwarps + warp;
