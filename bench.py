@@ -578,6 +578,10 @@ def per_config(w, B, headline_attn, workloads, peak) -> dict:
     res = {"peak_GBps": peak, "nominal_GBps": NOMINAL_HBM_GBS}
     res[w.name] = dict(entry(headline_attn), B=B)
     for name, r in (workloads or {}).items():
+        if name == "single_request":
+            res[name] = {n: {"us": v["us"], "context_len": v["context_len"]}
+                         for n, v in r.items()}
+            continue
         caps = wl.get(name).sm_caps_pct
         if not caps:
             res[name] = entry(r["all_sms"])
@@ -705,6 +709,38 @@ def sweep_workloads(args, dev, flush, peak):
     out_all = {}
     sms = pda.device_sm_count()
     stream = torch.cuda.current_stream(dev)
+
+    def time_attention(s, cap, nb):
+        out = torch.empty_like(s.q)
+        wsp = workspace_for(s, cap)
+        for _ in range(5):  # 5 warm-up launches, then the median of sweep_iters (50)
+            flush()
+            attention(s, out, cap, wsp)
+        ts = []
+        for _ in range(args.sweep_iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush()
+            a.record(stream)
+            attention(s, out, cap, wsp)
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        t = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e-3
+        gbs = nb / t / 1e9
+        return {"us": round(t * 1e6, 2), "GBps": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4),
+                "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
+
+    # One decode step of a single request (its latency, not bandwidth, is what matters):
+    # the first request of the 13B-shape and GQA recipes.
+    single = {}
+    for name in ("llama2_13b_b80", "gqa_skew_b256"):
+        s = wl.make_step(wl.get(name), device=dev, B=1)
+        r = time_attention(s, 0, step_bytes(s, [])["attention"])
+        single[name] = dict(r, context_len=int(s.context_lens_np[0]))
+        del s
+    out_all["single_request"] = single
+
     for name in ("tiny", "llama2_7b_b8", "llama2_13b_b80", "sm_sweep_b128", "llama2_13b_b80_fp8",
                  "gqa_skew_b256_fp8", "llama2_13b_b80_nvfp4", "gqa_skew_b256_nvfp4",
                  "gqa_skew_b256_f16", "gqa_skew_b256_bs64"):
@@ -716,26 +752,8 @@ def sweep_workloads(args, dev, flush, peak):
         caps = [0] + [int(math.ceil(p / 100 * sms)) for p in w.sm_caps_pct if p < 100]
         res_w = {}
         for cap in caps:
-            out = torch.empty_like(s.q)
-            wsp = workspace_for(s, cap)
-            for _ in range(5):  # 5 warm-up launches, then the median of sweep_iters (50)
-                flush()
-                attention(s, out, cap, wsp)
-            ts = []
-            for _ in range(args.sweep_iters):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                flush()
-                a.record(stream)
-                attention(s, out, cap, wsp)
-                b.record(stream)
-                ts.append((a, b))
-            torch.cuda.synchronize()
-            t = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e-3
-            gbs = nb["attention"] / t / 1e9
             key = "all_sms" if cap == 0 else f"sm_cap_{cap}"
-            res_w[key] = {"us": round(t * 1e6, 2), "GBps": round(gbs, 1),
-                          "frac_of_peak": round(gbs / peak, 4),
-                          "decode_tokens_per_s_per_layer": round(s.B / t, 1)}
+            res_w[key] = time_attention(s, cap, nb["attention"])
         res_w["bytes"] = nb["attention"]
         if not args.no_cpu_baseline:
             res_w["oracle"] = oracle_legs(w)

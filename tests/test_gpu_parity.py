@@ -255,6 +255,45 @@ def test_single_very_long_request_split_over_every_worker():
     assert_attention_close(out, ref, "B=1 L=32768", twin=fp32_twin(s))
 
 
+def _attention_direct(s, out, block_tables, max_context_len):
+    """The step's attention through the C ABI with a given table and length bound."""
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if s.w.kv == "nvfp4":
+        pda.paged_decode_attention_nvfp4(out, s.q, s.k_cache, s.v_cache, s.k_bscales,
+                                         s.v_bscales, block_tables, s.context_lens,
+                                         max_context_len, s.scale, s.k_scale, s.v_scale,
+                                         error_word=err)
+    elif s.w.kv == "fp8":
+        pda.paged_decode_attention_fp8(out, s.q, s.k_cache, s.v_cache, block_tables,
+                                       s.context_lens, max_context_len, s.scale, s.k_scale,
+                                       s.v_scale, error_word=err)
+    else:
+        pda.paged_decode_attention(out, s.q, s.k_cache, s.v_cache, block_tables,
+                                   s.context_lens, max_context_len, s.scale, error_word=err)
+    torch.cuda.synchronize()
+    return int(err.item())
+
+
+@pytest.mark.parametrize("name", ["gqa_skew_b256", "llama2_13b_b80", "gqa_skew_b256_fp8",
+                                  "gqa_skew_b256_nvfp4"])
+def test_lengths_far_below_the_declared_max(name):
+    """A table 2048 blocks wide and max_context_len 32768 let the host size the grid for the
+    whole chip, while the lengths hold a few tiles: the kernel keeps the few warps it needs
+    (8 tiles each at most), the others leave after the prologue, and the merges run over
+    the units that work."""
+    lens = np.array([16, 3, 40, 1, 17], np.int32)
+    s = wl.make_step(variant(name, B=len(lens)), device=DEV, lengths=lens)
+    ref, st, _, _ = oracle_full_step(s, append=False)
+    assert st == 0
+    wide = torch.full((s.B, 2048), -1, dtype=torch.int32, device=DEV)
+    wide[:, :s.max_blocks] = s.block_tables
+    out = torch.empty_like(s.q)
+    out32 = torch.empty(s.q.shape, dtype=torch.float32, device=DEV)
+    assert _attention_direct(s, out, wide, 32768) == 0
+    assert _attention_direct(s, out32, wide, 32768) == 0
+    assert_attention_close(out, ref, f"{name} short lengths, max 32768", twin=out32)
+
+
 def test_many_one_block_requests():
     lens = np.random.default_rng(3).integers(1, 17, size=600).astype(np.int32)
     w = variant("gqa_skew_b256", B=600)
