@@ -21,9 +21,9 @@
  *    contiguous or ordered, and several requests may share blocks (same page, sec. 2.2
  *    step 2 and sec. 2.3). Entries past a request's last block are never read.
  *  - Query head h reads kv-head h / (H / H_kv) (grouped-query attention, contiguous groups).
- *  - Every call is asynchronous on `stream` and never synchronises the host. Calls other
- *    than pda_paged_decode_attention_noalloc make no allocation, so a sequence of them can
- *    be captured in a CUDA graph once each kernel has been launched outside capture.
+ *  - Every call is asynchronous on `stream`, never synchronises the host and allocates no
+ *    device memory. A sequence of the calls other than pda_paged_decode_attention_noalloc
+ *    can be captured in a CUDA graph once each kernel has been launched outside capture.
  *  - Host-checkable errors (null pointers, bad sizes, unsupported dtypes or shapes,
  *    misaligned pointers) return a status before anything is launched. Errors in device
  *    data (a block id or slot out of range, a context length beyond capacity) cannot be
@@ -270,8 +270,7 @@ pda_status pda_paged_decode_attention_nvfp4(void* out, const void* q, const void
  *    On a 152-SM GB300 this admits every supported shape with H / H_kv <= 4 at D = 128
  *    (about 5 MB) and rejects H / H_kv = 8 at D = 128 (about 10 MB).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *    with that device current) and caches it; make that first call before any stream
- *    capture on that device.
+ *    with that device current) and caches it for later calls.
  *  - Every call shares the one array, which keeps the previous call's contents: those of a
  *    call of another shape, or of one that stopped early with PDA_DEVERR_TIMEOUT. Partial
  *    results are written before they are read. The per-segment arrival counters at the

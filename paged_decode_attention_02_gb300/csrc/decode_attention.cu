@@ -1428,9 +1428,11 @@ extern "C" pda_status pda_paged_decode_attention_nvfp4(
 
 // ------------------------------------------------------------------ no-allocation variant
 // Scratch for pda_paged_decode_attention_noalloc: a fixed device array in this module, for
-// callers that cannot allocate. Host code must not pass `g_noalloc_scratch` itself to a
-// kernel (on the host it names a host-side shadow, not device memory); it passes the
-// address cudaGetSymbolAddress returns for the current device.
+// callers that may not allocate device memory while they run: a plugin whose host
+// framework owns all device memory and hands it only inputs and outputs, or a serving loop
+// that forbids allocation once it has started. Host code must not pass `g_noalloc_scratch`
+// itself to a kernel (on the host it names a host-side shadow, not device memory); it
+// passes the address cudaGetSymbolAddress returns for the current device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PDA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
