@@ -83,12 +83,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and trailing blanks, so that editing a comment
+    does not change the kernel's hash."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_sha() -> str:
+    """Hash of the attention kernel's code (its sources without comments, and the build
+    options), which names the kernel an ncu summary under profiles/ was taken on."""
     h = hashlib.sha256()
     h.update(os.environ.get("PDA_NVCC_DEFINES", "").encode())  # build options change the code
     for p in ATTN_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
