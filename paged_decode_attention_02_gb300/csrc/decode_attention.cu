@@ -303,8 +303,9 @@ struct WarpAttn {
       }
       tmax = fmaxf(tmax, part[r]);
     }
+    // lanes cl and cl ^ m for m < DUP hold the same scores, so the max skips those masks
 #pragma unroll
-    for (int mask = LPH / 2; mask >= 1; mask >>= 1)
+    for (int mask = LPH / 2; mask >= DUP; mask >>= 1)
       tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, mask));
 #pragma unroll
     for (int mask = LPR; mask < 32; mask <<= 1)
