@@ -305,6 +305,21 @@ def test_many_one_block_requests():
     assert_attention_close(out, ref, "600 one-block requests", twin=fp32_twin(s))
 
 
+@pytest.mark.parametrize("name", ["gqa_skew_b256", "gqa_skew_b256_fp8", "gqa_skew_b256_nvfp4"])
+def test_largest_batch_every_output(name):
+    """The largest batch a call takes (8192 requests of 1 to 48 tokens). Its prefix table
+    fills 32 KB of shared memory, so blocks run fewer warps than usual; 65,536 short
+    (request, kv-head) segments, many cut by unit boundaries. Every output against the
+    oracle."""
+    lens = np.random.default_rng(11).integers(1, 49, size=8192).astype(np.int32)
+    s = wl.make_step(variant(name, B=8192), device=DEV, lengths=lens)
+    ref, st, _, _ = oracle_full_step(s)
+    assert st == 0
+    out, err = gpu_step(s)
+    assert err == 0
+    assert_attention_close(out, ref, f"{name} B=8192", twin=fp32_twin(s))
+
+
 def test_unused_rows_poisoned_with_nan_are_never_read():
     lens = np.array([5, 16, 17, 40, 1, 100], np.int32)
     s = wl.make_step("llama2_13b_b80", device=DEV, lengths=lens, B=6, poison_unused=True)
