@@ -186,6 +186,8 @@ SHAPES = [  # (dtype, D, H, H_kv)
     ("f32", 64, 8, 8), ("f32", 64, 8, 2), ("f32", 128, 8, 8), ("f32", 128, 16, 2),
     ("f16", 128, 32, 8), ("f16", 128, 40, 40), ("f16", 128, 12, 3), ("f16", 64, 16, 4),
     ("f16", 64, 8, 8),
+    # one kv-head for all query heads (multi-query attention)
+    ("bf16", 128, 8, 1), ("bf16", 128, 1, 1), ("f16", 64, 4, 1),
 ]
 
 
@@ -549,7 +551,8 @@ def test_unpack_bad_block_is_skipped_with_error_bit():
 # one kv-head per tile on the tensor cores for G = 8 (32/4) or odd H_kv with G >= 2 (12/3,
 # 6/3), CUDA cores for odd H_kv with G = 1 (5/5); D = 64: CUDA cores.
 FP8_SHAPES = [(128, 32, 32), (128, 32, 16), (128, 32, 8), (128, 32, 4), (128, 12, 3),
-              (128, 6, 3), (128, 5, 5), (64, 16, 16), (64, 16, 4)]
+              (128, 6, 3), (128, 5, 5), (64, 16, 16), (64, 16, 4),
+              (128, 8, 1), (128, 2, 1), (128, 1, 1)]  # the last three: one kv-head
 
 
 @pytest.mark.parametrize("D,H,H_kv", FP8_SHAPES)
@@ -617,7 +620,8 @@ def test_fp8_entry_rejects_plain_caches_and_base_entry_rejects_fp8():
 
 # ------------------------------------------------------------------ NVFP4 KV cache
 NVFP4_SHAPES = [(128, 32, 32), (128, 32, 8), (128, 32, 16), (128, 16, 2), (128, 64, 8),
-                (128, 12, 3), (128, 5, 5), (64, 16, 4), (64, 16, 16)]
+                (128, 12, 3), (128, 5, 5), (64, 16, 4), (64, 16, 16),
+                (128, 4, 1), (128, 1, 1)]  # the last two: one kv-head
 
 
 @pytest.mark.parametrize("D,H,H_kv", NVFP4_SHAPES)
